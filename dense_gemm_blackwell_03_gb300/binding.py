@@ -1,0 +1,291 @@
+"""ctypes binding of ``libbwgemm.so`` (C ABI in ``include/bwgemm.h``).
+
+Argument marshalling only: torch tensors are turned into device pointers,
+element strides and the current CUDA stream, and every call goes straight to
+the library, whose sm_103a kernels do all the arithmetic.  If the library
+cannot be loaded the calls raise; there is no host-side fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+BF16 = 0
+FP16 = 1
+
+STATUS_NAMES = {
+    0: "BWGEMM_OK",
+    1: "BWGEMM_ERR_INVALID_ARG",
+    2: "BWGEMM_ERR_ALIGNMENT",
+    3: "BWGEMM_ERR_UNSUPPORTED",
+    4: "BWGEMM_ERR_NO_DEVICE",
+    5: "BWGEMM_ERR_CUDA",
+    6: "BWGEMM_ERR_TIMEOUT",
+    7: "BWGEMM_ERR_WORKSPACE",
+}
+
+# every symbol include/bwgemm.h declares
+EXPORTED = [
+    "bwgemm_default_options", "bwgemm_create_plan", "bwgemm_destroy", "bwgemm_run",
+    "bwgemm_run_host", "bwgemm_get_status", "bwgemm_last_device_status", "bwgemm_check_args",
+    "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
+    "bwgemm_status_string", "bwgemm_version",
+]
+
+
+class BwgemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        name = STATUS_NAMES.get(self.status, f"status {status}")
+        super().__init__(f"{what}: {name}" if what else name)
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [
+        ("variant", ctypes.c_int32),
+        ("tile_n", ctypes.c_int32),
+        ("split_k", ctypes.c_int32),
+        ("raster_group", ctypes.c_int32),
+        ("max_ctas", ctypes.c_int32),
+        ("stall_kblock", ctypes.c_int32),
+        ("timeout_ns", ctypes.c_uint64),
+        ("workspace_bytes", ctypes.c_uint64),
+        ("reserved", ctypes.c_int32 * 8),
+    ]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [
+        ("variant", ctypes.c_int32),
+        ("tile_m", ctypes.c_int32),
+        ("tile_n", ctypes.c_int32),
+        ("tile_k", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
+        ("split_k", ctypes.c_int32),
+        ("raster_group", ctypes.c_int32),
+        ("num_tiles", ctypes.c_int32),
+        ("num_units", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    here = os.path.dirname(os.path.abspath(__file__))
+    return os.environ.get("BWGEMM_LIBRARY", os.path.join(here, "_build", "libbwgemm.so"))
+
+
+def load_library(build_if_missing: bool = False):
+    """Load ``libbwgemm.so`` (building it first when asked and missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise BwgemmError(4, f"{path} not built (run __graft_entry__.build())")
+            from . import build as _build
+            path = _build.build()
+        lib = ctypes.CDLL(path)
+        vp = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        i32 = ctypes.c_int32
+        st = ctypes.c_int
+        lib.bwgemm_default_options.argtypes = [ctypes.POINTER(PlanOptions)]
+        lib.bwgemm_default_options.restype = None
+        lib.bwgemm_create_plan.argtypes = [ctypes.POINTER(vp), ctypes.c_int, ctypes.POINTER(PlanOptions)]
+        lib.bwgemm_create_plan.restype = st
+        lib.bwgemm_destroy.argtypes = [vp]
+        lib.bwgemm_destroy.restype = st
+        gemm_args = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_int, vp]
+        lib.bwgemm_run.argtypes = gemm_args
+        lib.bwgemm_run.restype = st
+        lib.bwgemm_run_host.argtypes = gemm_args
+        lib.bwgemm_run_host.restype = st
+        lib.bwgemm_get_status.argtypes = [vp, vp]
+        lib.bwgemm_get_status.restype = st
+        lib.bwgemm_last_device_status.argtypes = [vp]
+        lib.bwgemm_last_device_status.restype = ctypes.c_uint32
+        lib.bwgemm_check_args.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_int]
+        lib.bwgemm_check_args.restype = st
+        lib.bwgemm_select_config.argtypes = [i32, i32, i64, i64, i64, ctypes.c_int,
+                                             ctypes.POINTER(PlanOptions), ctypes.POINTER(Config)]
+        lib.bwgemm_select_config.restype = st
+        lib.bwgemm_plan_last_config.argtypes = [vp, ctypes.POINTER(Config)]
+        lib.bwgemm_plan_last_config.restype = st
+        lib.bwgemm_plan_launch_count.argtypes = [vp]
+        lib.bwgemm_plan_launch_count.restype = ctypes.c_uint64
+        lib.bwgemm_status_string.argtypes = [ctypes.c_int]
+        lib.bwgemm_status_string.restype = ctypes.c_char_p
+        lib.bwgemm_version.argtypes = []
+        lib.bwgemm_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def make_options(**kw) -> PlanOptions:
+    lib = load_library()
+    o = PlanOptions()
+    lib.bwgemm_default_options(ctypes.byref(o))
+    for k, v in kw.items():
+        if v is None:
+            continue
+        if not hasattr(o, k) or k == "reserved":
+            raise TypeError(f"unknown plan option {k!r}")
+        setattr(o, k, v)
+    return o
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    raise TypeError(f"bwgemm takes bfloat16 or float16 tensors, got {t.dtype}")
+
+
+def _ld(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("operands must be K-major / row-major (unit stride along the last dim)")
+    return int(t.stride(0)) if t.shape[0] > 1 else max(int(t.shape[1]), 1)
+
+
+def select_config(num_sms: int, M: int, N: int, K: int, dtype: int = BF16, max_pairs: int = 0,
+                  **opts) -> dict:
+    """Host-only: the configuration a plan would choose (no GPU needed)."""
+    lib = load_library()
+    o = make_options(**opts)
+    cfg = Config()
+    rc = lib.bwgemm_select_config(num_sms, max_pairs, M, N, K, dtype, ctypes.byref(o), ctypes.byref(cfg))
+    if rc != 0:
+        raise BwgemmError(rc, "bwgemm_select_config")
+    return cfg.as_dict()
+
+
+def check_args(A_ptr, B_ptr, C_ptr, M, N, K, lda, ldb, ldc, dtype=BF16) -> int:
+    """Host-only: the status bwgemm_run would return for these arguments."""
+    return int(load_library().bwgemm_check_args(A_ptr, B_ptr, C_ptr, M, N, K, lda, ldb, ldc, dtype))
+
+
+class Plan:
+    """A bwgemm plan on one CUDA device (see ``bwgemm_create_plan``)."""
+
+    def __init__(self, device: int | None = None, **opts):
+        import torch
+        self.lib = load_library()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = int(device)
+        self.options = make_options(**opts)
+        h = ctypes.c_void_p()
+        rc = self.lib.bwgemm_create_plan(ctypes.byref(h), self.device, ctypes.byref(self.options))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_create_plan")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.bwgemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @staticmethod
+    def _stream_handle(stream):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(int(stream.cuda_stream))
+
+    def run_raw(self, A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int, lda: int,
+                ldb: int, ldc: int, dtype: int, stream_ptr: int | None) -> int:
+        """Direct call of ``bwgemm_run`` with raw pointers; returns the status code."""
+        return int(self.lib.bwgemm_run(self.handle, A_ptr, B_ptr, C_ptr, M, N, K, lda, ldb, ldc,
+                                       dtype, stream_ptr))
+
+    def gemm(self, A, B, out=None, stream=None):
+        """``out = A @ B.T`` for CUDA bf16/fp16 tensors A (M x K) and B (N x K)."""
+        import torch
+        dt = _dtype_code(A)
+        if B.dtype != A.dtype:
+            raise TypeError("A and B must have the same dtype")
+        if not (A.is_cuda and B.is_cuda):
+            raise ValueError("A and B must be CUDA tensors (bwgemm has no host path)")
+        M, K = A.shape
+        N, Kb = B.shape
+        if Kb != K:
+            raise ValueError(f"K mismatch: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+        if out is None:
+            out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+        elif out.dtype != A.dtype or tuple(out.shape) != (M, N) or not out.is_cuda:
+            raise ValueError("out must be an M x N CUDA tensor of the operands' dtype")
+        rc = self.lib.bwgemm_run(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                                 _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_run")
+        return out
+
+    def gemm_host(self, A, B, out=None, stream=None):
+        """``bwgemm_run_host``: A, B, out are CPU tensors (pinned for speed)."""
+        import torch
+        dt = _dtype_code(A)
+        M, K = A.shape
+        N, _ = B.shape
+        if out is None:
+            out = torch.empty((M, N), dtype=A.dtype)
+        rc = self.lib.bwgemm_run_host(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N,
+                                      K, _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_run_host")
+        return out
+
+    def status(self, stream=None) -> int:
+        """``bwgemm_get_status``: synchronises the stream, returns and clears the status."""
+        return int(self.lib.bwgemm_get_status(self.handle, self._stream_handle(stream)))
+
+    def last_device_status(self) -> int:
+        return int(self.lib.bwgemm_last_device_status(self.handle))
+
+    def last_config(self) -> dict:
+        cfg = Config()
+        rc = self.lib.bwgemm_plan_last_config(self.handle, ctypes.byref(cfg))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_plan_last_config")
+        return cfg.as_dict()
+
+    def launch_count(self) -> int:
+        return int(self.lib.bwgemm_plan_launch_count(self.handle))
+
+
+_plans: dict = {}
+
+
+def gemm(A, B, out=None, stream=None):
+    """``A @ B.T`` with a cached default plan per device."""
+    dev = A.device.index if A.device.index is not None else 0
+    plan = _plans.get(dev)
+    if plan is None:
+        plan = _plans[dev] = Plan(dev)
+    return plan.gemm(A, B, out=out, stream=stream)

@@ -1,0 +1,371 @@
+// api.cpp -- plans, tensor maps and launches behind the C ABI of bwgemm.h.
+//
+// TMA descriptors are built on the host (shape, strides, box, 128B swizzle,
+// zero fill outside the tensor), the way both pages create them before the
+// launch ("Writing a Blackwell GEMM by hand", TMA section: bounds and strides
+// live in the descriptor; "Matrix Multiplication on NVIDIA's Blackwell",
+// Kernel 2: host-side create_tma_tile).
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+using namespace bwgemm;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+struct TmapSlot {
+    const void* ptr = nullptr;
+    int64_t inner = 0, outer = 0, ld = 0;
+    int dtype = -1;
+    uint32_t box_inner = 0, box_outer = 0;
+    int swizzle = -1;
+    bool valid = false;
+    CUtensorMap map;
+};
+
+// Build (or reuse) a 2-D tensor map of a row-major matrix: `outer` rows of
+// `inner` elements, `ld` elements apart.
+bwgemm_status_t get_tmap(TmapSlot& s, const void* ptr, int dtype, int64_t inner, int64_t outer,
+                         int64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
+{
+    if (s.valid && s.ptr == ptr && s.inner == inner && s.outer == outer && s.ld == ld &&
+        s.dtype == dtype && s.box_inner == box_inner && s.box_outer == box_outer &&
+        s.swizzle == int(swz))
+        return BWGEMM_OK;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return BWGEMM_ERR_NO_DEVICE;
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    s.valid = false;
+    const CUresult r = enc(&s.map,
+                           dtype == BWGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           2, const_cast<void*>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return BWGEMM_ERR_CUDA;
+    s.ptr = ptr;
+    s.inner = inner;
+    s.outer = outer;
+    s.ld = ld;
+    s.dtype = dtype;
+    s.box_inner = box_inner;
+    s.box_outer = box_outer;
+    s.swizzle = int(swz);
+    s.valid = true;
+    return BWGEMM_OK;
+}
+
+// Makes the plan's device current for the lifetime of the guard.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            prev = -1;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        if (ok && prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct bwgemm_plan_s {
+    int device = 0;
+    int num_sms = 0;
+    int max_active[kNumVariants] = {};
+    bwgemm_plan_options_t opts;
+    uint32_t* d_status = nullptr;
+    uint8_t* d_workspace = nullptr;
+    uint64_t workspace_bytes = 0;
+    TmapSlot tmaps[3];
+    bwgemm_config_t last;
+    uint64_t launches = 0;
+    uint32_t last_status_bits = 0;
+    // device staging buffers of bwgemm_run_host
+    void* h2d[3] = {nullptr, nullptr, nullptr};
+    size_t h2d_cap[3] = {0, 0, 0};
+};
+
+namespace {
+
+bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        bwgemm_dtype_t dtype, cudaStream_t stream)
+{
+    bwgemm_status_t st = bwgemm_check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype);
+    if (st != BWGEMM_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return BWGEMM_OK;
+    if (K == 0) {  // empty sum: C = 0
+        if (cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+        return BWGEMM_OK;
+    }
+    Selection sel;
+    st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256)], M, N, K, plan->opts,
+                       plan->workspace_bytes, &sel);
+    if (st != BWGEMM_OK)
+        return st;
+    const Variant& v = kVariants[sel.variant_idx];
+    const uint32_t b_rows = uint32_t(v.cg == 1 ? v.bn : v.bn / 2);
+    if ((st = get_tmap(plan->tmaps[0], A, dtype, K, M, lda, kTileK, kRowsPerCta,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK)
+        return st;
+    if ((st = get_tmap(plan->tmaps[1], B, dtype, K, N, ldb, kTileK, b_rows,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK)
+        return st;
+    if ((st = get_tmap(plan->tmaps[2], C, dtype, N, M, ldc, kStoreCols, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B)) != BWGEMM_OK)
+        return st;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.M = int32_t(M);
+    p.N = int32_t(N);
+    p.K = int32_t(K);
+    p.num_m_blocks = sel.num_m_blocks;
+    p.num_n_blocks = sel.num_n_blocks;
+    p.num_k_blocks = sel.num_k_blocks;
+    p.num_tiles = sel.cfg.num_tiles;
+    p.split_k = sel.cfg.split_k;
+    p.num_units = sel.cfg.num_units;
+    p.raster_group = sel.cfg.raster_group;
+    p.dtype = int32_t(dtype);
+    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
+    p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
+    p.status = plan->d_status;
+    p.tile_sems = reinterpret_cast<uint32_t*>(plan->d_workspace);
+    p.partials = reinterpret_cast<float*>(plan->d_workspace + kCounterRegionBytes);
+    p.stall_kblock = plan->opts.stall_kblock;
+
+    const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
+                                           plan->tmaps[2].map, p, sel.cfg.grid, stream);
+    if (err != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    plan->last = sel.cfg;
+    plan->launches += 1;
+    return BWGEMM_OK;
+}
+
+bwgemm_status_t grow(void*& buf, size_t& cap, size_t need)
+{
+    if (cap >= need)
+        return BWGEMM_OK;
+    if (buf) {
+        cudaFree(buf);
+        buf = nullptr;
+        cap = 0;
+    }
+    if (cudaMalloc(&buf, need) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    cap = need;
+    return BWGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bwgemm_status_t bwgemm_create_plan(bwgemm_plan_t* out, int device,
+                                   const bwgemm_plan_options_t* opts)
+{
+    if (!out)
+        return BWGEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    bwgemm_plan_options_t o;
+    if (opts)
+        o = *opts;
+    else
+        bwgemm_default_options(&o);
+    for (int32_t r : o.reserved)
+        if (r != 0)
+            return BWGEMM_ERR_INVALID_ARG;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+        cudaGetLastError();
+        return BWGEMM_ERR_NO_DEVICE;
+    }
+    if (device < 0 || device >= count)
+        return BWGEMM_ERR_INVALID_ARG;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    if (major != 10 || minor != 3)
+        return BWGEMM_ERR_UNSUPPORTED;  // sm_103 only: no other code path exists
+    if (!encode_fn())
+        return BWGEMM_ERR_NO_DEVICE;
+
+    DeviceGuard guard(device);
+    if (!guard.ok)
+        return BWGEMM_ERR_CUDA;
+    bwgemm_plan_s* plan = new (std::nothrow) bwgemm_plan_s();
+    if (!plan)
+        return BWGEMM_ERR_CUDA;
+    plan->device = device;
+    plan->num_sms = sms;
+    plan->opts = o;
+    plan->workspace_bytes = o.workspace_bytes ? o.workspace_bytes : (64ull << 20);
+    std::memset(&plan->last, 0, sizeof(plan->last));
+    for (int i = 0; i < kNumVariants; ++i) {
+        if (variant_max_active(i, &plan->max_active[i]) != cudaSuccess || plan->max_active[i] <= 0) {
+            cudaGetLastError();
+            delete plan;
+            return BWGEMM_ERR_UNSUPPORTED;  // kernel image does not load or does not fit
+        }
+    }
+    if (cudaMalloc(&plan->d_status, 256) != cudaSuccess ||
+        cudaMalloc(&plan->d_workspace, plan->workspace_bytes) != cudaSuccess ||
+        cudaMemset(plan->d_status, 0, 256) != cudaSuccess ||
+        cudaMemset(plan->d_workspace, 0, kCounterRegionBytes) != cudaSuccess) {
+        cudaFree(plan->d_status);
+        cudaFree(plan->d_workspace);
+        delete plan;
+        return BWGEMM_ERR_CUDA;
+    }
+    *out = plan;
+    return BWGEMM_OK;
+}
+
+bwgemm_status_t bwgemm_destroy(bwgemm_plan_t plan)
+{
+    if (!plan)
+        return BWGEMM_OK;
+    DeviceGuard guard(plan->device);
+    cudaDeviceSynchronize();
+    cudaFree(plan->d_status);
+    cudaFree(plan->d_workspace);
+    for (void* b : plan->h2d)
+        if (b)
+            cudaFree(b);
+    delete plan;
+    return BWGEMM_OK;
+}
+
+bwgemm_status_t bwgemm_run(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           bwgemm_dtype_t dtype, void* stream)
+{
+    if (!plan)
+        return BWGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok)
+        return BWGEMM_ERR_CUDA;
+    return enqueue(plan, A, B, C, M, N, K, lda, ldb, ldc, dtype, static_cast<cudaStream_t>(stream));
+}
+
+bwgemm_status_t bwgemm_get_status(bwgemm_plan_t plan, void* stream)
+{
+    if (!plan)
+        return BWGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok)
+        return BWGEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    uint32_t bits = 0;
+    if (cudaMemcpy(&bits, plan->d_status, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    plan->last_status_bits = bits;
+    if (bits == 0)
+        return BWGEMM_OK;
+    // clear the word and re-arm the split-K arrival counters an aborted launch may have left
+    if (cudaMemset(plan->d_status, 0, sizeof(bits)) != cudaSuccess ||
+        cudaMemset(plan->d_workspace, 0, kCounterRegionBytes) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    return BWGEMM_ERR_TIMEOUT;
+}
+
+uint32_t bwgemm_last_device_status(bwgemm_plan_t plan) { return plan ? plan->last_status_bits : 0u; }
+
+bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const void* B_host,
+                                void* C_host, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, void* stream)
+{
+    if (!plan)
+        return BWGEMM_ERR_INVALID_ARG;
+    // host operands need no alignment; the device copies are packed with
+    // leading dimensions rounded up to 8 elements
+    if (dtype != BWGEMM_BF16 && dtype != BWGEMM_FP16)
+        return BWGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < N)
+        return BWGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return BWGEMM_OK;
+    if (!C_host || (K > 0 && (!A_host || !B_host)))
+        return BWGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok)
+        return BWGEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t dlda = std::max<int64_t>((K + 7) / 8 * 8, 8);
+    const int64_t dldc = (N + 7) / 8 * 8;
+    bwgemm_status_t st;
+    if ((st = grow(plan->h2d[0], plan->h2d_cap[0], size_t(M) * dlda * 2)) != BWGEMM_OK ||
+        (st = grow(plan->h2d[1], plan->h2d_cap[1], size_t(N) * dlda * 2)) != BWGEMM_OK ||
+        (st = grow(plan->h2d[2], plan->h2d_cap[2], size_t(M) * dldc * 2)) != BWGEMM_OK)
+        return st;
+    if (K > 0) {
+        if (cudaMemcpy2DAsync(plan->h2d[0], size_t(dlda) * 2, A_host, size_t(lda) * 2, size_t(K) * 2,
+                              size_t(M), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpy2DAsync(plan->h2d[1], size_t(dlda) * 2, B_host, size_t(ldb) * 2, size_t(K) * 2,
+                              size_t(N), cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+    }
+    st = enqueue(plan, plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N, K, dlda, dlda, dldc, dtype, s);
+    if (st != BWGEMM_OK)
+        return st;
+    if (cudaMemcpy2DAsync(C_host, size_t(ldc) * 2, plan->h2d[2], size_t(dldc) * 2, size_t(N) * 2,
+                          size_t(M), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    return bwgemm_get_status(plan, stream);
+}
+
+bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out)
+{
+    if (!plan || !out)
+        return BWGEMM_ERR_INVALID_ARG;
+    *out = plan->last;
+    return BWGEMM_OK;
+}
+
+uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan) { return plan ? plan->launches : 0u; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// internal.h -- declarations shared by the library's host-side translation units.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bwgemm.h"
+#include "kernel_params.h"
+
+namespace bwgemm {
+
+// Compiled kernel variants: (CTA group, BN, ring stages).  Every variant keeps
+// the ring at 192 KiB of shared memory plus 16 KiB of epilogue staging.
+struct Variant {
+    int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
+    int bn;      // columns of C per unit (= MMA N)
+    int stages;  // shared-memory ring depth
+};
+
+constexpr Variant kVariants[] = {
+    {1, 256, 4},
+    {1, 128, 6},
+    {2, 256, 6},
+    {2, 128, 8},
+};
+constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+
+// Index into kVariants, or -1.
+int find_variant(int cg, int bn);
+
+// Dynamic shared memory bytes of a variant.
+int variant_smem_bytes(int idx);
+
+// Launch variant `idx` with `grid` CTAs (a multiple of its CTA group).
+cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const GemmParams& p, int grid, cudaStream_t stream);
+
+// Co-resident clusters (CTA pairs for cg == 2, CTAs for cg == 1) of variant
+// `idx` on the current device.
+cudaError_t variant_max_active(int idx, int* out);
+
+// Sizes of the split-K workspace regions.
+constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) arrival counters
+
+struct Selection {
+    bwgemm_config_t cfg;
+    int variant_idx;
+    int num_m_blocks, num_n_blocks, num_k_blocks;
+};
+
+// Host-only configuration choice (also behind bwgemm_select_config).
+bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, int64_t K,
+                              const bwgemm_plan_options_t& opts, uint64_t workspace_bytes,
+                              Selection* out);
+
+}  // namespace bwgemm

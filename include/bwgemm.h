@@ -1,0 +1,189 @@
+/*
+ * bwgemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library libbwgemm.so.
+ *
+ * The operation (the one all the source pages build):
+ *
+ *     C[M x N] = A[M x K] * B[N x K]^T
+ *
+ *   A, B : bf16 or fp16, both stored K-major (row-major A; B stored N x K,
+ *          i.e. "B already transposed" -- "Matrix Multiplication on NVIDIA's
+ *          Blackwell", optimisation roadmap section and the naive Kernel 1,
+ *          which reads b[col, k]).
+ *   accumulation in fp32 ("BF16 in and out, converted to FP32 to accumulate",
+ *          same page, Kernel 1 section; the CuTeDSL post's K-loop,
+ *          "Writing a Blackwell GEMM by hand", step 1 equation).
+ *   C    : same type as A and B, rounded to nearest even from fp32.
+ *
+ * All sizes and leading dimensions are in elements.  Matrices are row-major
+ * with row strides lda / ldb / ldc (lda >= K, ldb >= K, ldc >= N).
+ *
+ * Alignment (the TMA rules the kernels rely on): A, B, C 16-byte aligned;
+ * lda, ldb, ldc multiples of 8 elements.  Violations return
+ * BWGEMM_ERR_ALIGNMENT; nothing is launched.
+ *
+ * Threading: a plan may be used from one host thread at a time and on one
+ * stream at a time (its split-K workspace and status word are shared by its
+ * launches).  Different plans are independent.
+ *
+ * Nothing is thrown across this boundary; every entry point returns a status.
+ */
+#ifndef BWGEMM_H
+#define BWGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BWGEMM_VERSION_MAJOR 0
+#define BWGEMM_VERSION_MINOR 1
+
+typedef struct bwgemm_plan_s* bwgemm_plan_t;
+
+typedef enum {
+    BWGEMM_BF16 = 0, /* bfloat16 inputs and output */
+    BWGEMM_FP16 = 1  /* IEEE binary16 inputs and output */
+} bwgemm_dtype_t;
+
+typedef enum {
+    BWGEMM_OK = 0,
+    BWGEMM_ERR_INVALID_ARG = 1, /* bad size, stride, dtype, NULL pointer or handle      */
+    BWGEMM_ERR_ALIGNMENT = 2,   /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    BWGEMM_ERR_UNSUPPORTED = 3, /* device is not sm_103 / size beyond the supported range */
+    BWGEMM_ERR_NO_DEVICE = 4,   /* no CUDA device / driver                                */
+    BWGEMM_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed                   */
+    BWGEMM_ERR_TIMEOUT = 6,     /* a device-side wait ran out (see bwgemm_get_status)     */
+    BWGEMM_ERR_WORKSPACE = 7    /* split-K workspace too small for the forced options     */
+} bwgemm_status_t;
+
+typedef enum {
+    BWGEMM_VARIANT_AUTO = 0, /* choose from the shape                                  */
+    BWGEMM_VARIANT_1SM = 1,  /* one CTA per tile: 128 x BN tiles, tcgen05 cta_group::1 */
+    BWGEMM_VARIANT_2SM = 2   /* CTA pair per tile: 256 x BN tiles, cta_group::2        */
+} bwgemm_variant_t;
+
+/* Plan options.  Zero means "choose automatically" for every field; get the
+ * defaults with bwgemm_default_options(). */
+typedef struct {
+    int32_t variant;          /* bwgemm_variant_t                                       */
+    int32_t tile_n;           /* 0, 128 or 256: columns of C per work unit              */
+    int32_t split_k;          /* 0 = auto, 1 = off, s >= 2: s K-slices per tile         */
+    int32_t raster_group;     /* 0 = auto; m-blocks walked before stepping along N      */
+    int32_t max_ctas;         /* 0 = fill the GPU; else cap on the persistent grid      */
+    int32_t stall_kblock;     /* test hook, keep -1: the producer of CTA 0 never fills
+                                 this k-block of its first unit, so a bounded wait runs
+                                 out and the call reports BWGEMM_ERR_TIMEOUT            */
+    uint64_t timeout_ns;      /* bound on every device-side wait; 0 = 4 s               */
+    uint64_t workspace_bytes; /* split-K workspace owned by the plan; 0 = 64 MiB        */
+    int32_t reserved[8];      /* must be zero                                            */
+} bwgemm_plan_options_t;
+
+/* The launch configuration chosen for a shape (for inspection and tests). */
+typedef struct {
+    int32_t variant;      /* BWGEMM_VARIANT_1SM or BWGEMM_VARIANT_2SM            */
+    int32_t tile_m;       /* rows of C per work unit (128 or 256)                */
+    int32_t tile_n;       /* columns of C per work unit                          */
+    int32_t tile_k;       /* K elements per pipeline stage (64)                  */
+    int32_t stages;       /* depth of the shared-memory ring                     */
+    int32_t split_k;      /* K slices per tile (1 = none)                        */
+    int32_t raster_group; /* m-blocks per raster group                           */
+    int32_t num_tiles;    /* output tiles                                        */
+    int32_t num_units;    /* tiles x split_k                                     */
+    int32_t grid;         /* CTAs launched (persistent)                          */
+    int64_t workspace_bytes; /* split-K bytes used by this shape                 */
+} bwgemm_config_t;
+
+/* Fill *opts with the defaults (all automatic, stall_kblock = -1). */
+void bwgemm_default_options(bwgemm_plan_options_t* opts);
+
+/*
+ * Create a plan on CUDA device `device` (an ordinal; the library makes it
+ * current for the calls it makes).  Checks that the device is compute
+ * capability 10.3 (sm_103) and returns BWGEMM_ERR_UNSUPPORTED otherwise --
+ * there is no fallback path.  Allocates the plan's device status word and
+ * split-K workspace.  `opts` may be NULL (defaults).  On failure *plan is NULL.
+ */
+bwgemm_status_t bwgemm_create_plan(bwgemm_plan_t* plan, int device,
+                                   const bwgemm_plan_options_t* opts);
+
+/* Free a plan and its device memory.  NULL is accepted.  Synchronises the
+ * device first, so no launch of the plan may still be running. */
+bwgemm_status_t bwgemm_destroy(bwgemm_plan_t plan);
+
+/*
+ * C = A * B^T on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *
+ *   A : device pointer, M x K, row stride lda (read only)
+ *   B : device pointer, N x K, row stride ldb (read only; may alias A)
+ *   C : device pointer, M x N, row stride ldc (written; must not overlap A or B)
+ *
+ * The caller owns A, B and C and keeps them alive until the stream reaches
+ * the launch.  Asynchronous: returns after enqueueing one kernel (none when
+ * M == 0 or N == 0; a zero fill of C when K == 0, the empty sum).  No host
+ * synchronisation and no device allocation, so it may be captured in a CUDA
+ * graph.  Argument errors are returned synchronously and launch nothing.
+ * Device-side timeouts are reported by bwgemm_get_status().
+ */
+bwgemm_status_t bwgemm_run(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           bwgemm_dtype_t dtype, void* stream);
+
+/*
+ * Same product with HOST operands: copies A and B (host memory, pinned for
+ * full speed) to plan-owned device buffers, runs the GEMM, copies C back to
+ * host memory, and synchronises `stream` before returning.  The device
+ * buffers grow on demand and are kept for later calls.  Returns the device
+ * status of the launch (as bwgemm_get_status would).
+ */
+bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const void* B_host,
+                                void* C_host, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device status word:
+ * BWGEMM_OK, or BWGEMM_ERR_TIMEOUT when a bounded device-side wait of an
+ * earlier launch ran out (that launch's C is then undefined), or
+ * BWGEMM_ERR_CUDA.  Clearing also re-arms the split-K turn counters.
+ */
+bwgemm_status_t bwgemm_get_status(bwgemm_plan_t plan, void* stream);
+
+/* Raw device status bits of the last bwgemm_get_status() call (0 = fine). */
+uint32_t bwgemm_last_device_status(bwgemm_plan_t plan);
+
+/*
+ * Host-only argument check of a bwgemm_run() call (no device access):
+ * returns the status bwgemm_run would return for these arguments before
+ * launching anything.
+ */
+bwgemm_status_t bwgemm_check_args(const void* A, const void* B, const void* C, int64_t M,
+                                  int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                  bwgemm_dtype_t dtype);
+
+/*
+ * Host-only: the configuration a plan with `opts` (NULL = defaults) would
+ * pick for this shape on a GPU with `num_sms` SMs that can hold
+ * `max_pairs` co-resident CTA pairs (0 = num_sms / 2).  No device access.
+ */
+bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
+                                     int64_t K, bwgemm_dtype_t dtype,
+                                     const bwgemm_plan_options_t* opts, bwgemm_config_t* out);
+
+/* The configuration of the plan's most recent bwgemm_run / bwgemm_run_host. */
+bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out);
+
+/* Number of GEMM kernels the plan has enqueued since it was created. */
+uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);
+
+/* Static text for a status code ("unknown status" for anything else). */
+const char* bwgemm_status_string(bwgemm_status_t status);
+
+/* Library version as (major << 16) | minor. */
+int32_t bwgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BWGEMM_H */

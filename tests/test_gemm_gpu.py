@@ -1,0 +1,196 @@
+"""GPU parity: the sm_103a kernels through the C ABI against the CPU oracle.
+
+Small shapes are compared element by element over the whole output; the
+pages' full-size shapes (4096^3, Llama-3-70B prefill and decode linears,
+Gemma-3-27B-like and small-M tails) are compared on a seeded sample of 64
+full rows and 64 full columns of C, in the configuration the benchmark times.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_blackwell_03_gb300 import binding
+from dense_gemm_blackwell_03_gb300.workloads import SHAPES, bits_of, make_inputs, make_matrix
+from parity import compare, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+TORCH16 = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def plan():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    binding.load_library(build_if_missing=True)
+    p = binding.Plan(0)
+    yield p
+    assert p.status() == 0
+    p.close()
+
+
+def run_full(plan, A, B, dtype, exact=False, out=None):
+    C = plan.gemm(A, B, out=out)
+    assert plan.status() == 0
+    ref = oracle.gemm(bits_of(A), bits_of(B), dtype)
+    return compare(bits_of(C), ref, dtype, A.shape[1], exact=exact), C
+
+
+# ---------------------------------------------------------------- small shapes
+@pytest.mark.parametrize("variant", [1, 2])
+def test_square512_integers_bit_exact(variant):
+    s = SHAPES["square512_int"]
+    A, B = make_inputs(s, device="cuda")
+    with binding.Plan(0, variant=variant) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        assert p.last_config()["variant"] == variant
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_square512_normal(plan, dtype):
+    s = SHAPES["square512"].with_dtype(dtype)
+    A, B = make_inputs(s, device="cuda")
+    run_full(plan, A, B, dtype)
+
+
+@pytest.mark.parametrize("K", [16, 32, 48, 64, 80, 200, 1000])
+def test_k_steps_and_k_tails(plan, K):
+    # the first MMA overwrites the accumulator, later ones add (K = 16: one
+    # instruction); K not a multiple of 64 reads zeros past the end
+    A = make_matrix(256, K, "int2", seed=100 + K, device="cuda")
+    B = make_matrix(192, K, "int2", seed=200 + K, device="cuda")
+    run_full(plan, A, B, "bf16", exact=True)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 127, 129, 200, 255, 257, 300])
+def test_m_tails(plan, M):
+    A = make_matrix(M, 512, "int2", seed=300 + M, device="cuda")
+    B = make_matrix(320, 512, "int2", seed=400 + M, device="cuda")
+    run_full(plan, A, B, "bf16", exact=True)
+
+
+@pytest.mark.parametrize("N", [8, 40, 136, 264, 1000])
+def test_n_tails(plan, N):
+    A = make_matrix(384, 256, "normal", seed=500 + N, device="cuda")
+    B = make_matrix(N, 256, "normal", seed=600 + N, device="cuda")
+    run_full(plan, A, B, "bf16")
+
+
+def test_strided_operands_and_output(plan):
+    M, N, K = 300, 200, 328
+    A = make_matrix(M, K, "int2", seed=701, device="cuda", ld=K + 24)
+    B = make_matrix(N, K, "int2", seed=702, device="cuda", ld=K + 8)
+    Cbuf = torch.full((M, N + 40), 7.0, dtype=torch.bfloat16, device="cuda")
+    C = Cbuf[:, :N]
+    run_full(plan, A, B, "bf16", exact=True, out=C)
+    assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
+
+
+@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_every_variant(variant, tile_n, dtype):
+    A = make_matrix(520, 640, "normal", dtype, seed=800, device="cuda")
+    B = make_matrix(600, 640, "normal", dtype, seed=801, device="cuda")
+    with binding.Plan(0, variant=variant, tile_n=tile_n) as p:
+        run_full(p, A, B, dtype)
+        c = p.last_config()
+        assert (c["variant"], c["tile_n"]) == (variant, tile_n)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("split", [2, 3, 5])
+def test_split_k_exact_and_deterministic(variant, split):
+    A = make_matrix(256, 1600, "int2", seed=900, device="cuda")
+    B = make_matrix(512, 1600, "int2", seed=901, device="cuda")
+    with binding.Plan(0, variant=variant, split_k=split) as p:
+        _, C1 = run_full(p, A, B, "bf16", exact=True)
+        assert p.last_config()["split_k"] == split
+        C2 = p.gemm(A, B)
+        assert p.status() == 0
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+def test_split_k_normal_inputs():
+    A = make_matrix(200, 4096, "normal", seed=910, device="cuda")
+    B = make_matrix(384, 4096, "weight", seed=911, device="cuda")
+    with binding.Plan(0, split_k=4) as p:
+        run_full(p, A, B, "bf16")
+
+
+def test_persistent_grid_smaller_than_units():
+    # more work units than CTAs: every CTA walks several units, both TMEM
+    # accumulators and the ring wrap many times
+    A = make_matrix(1024, 512, "int2", seed=920, device="cuda")
+    B = make_matrix(1024, 512, "int2", seed=921, device="cuda")
+    for variant in (1, 2):
+        with binding.Plan(0, variant=variant, max_ctas=6) as p:
+            run_full(p, A, B, "bf16", exact=True)
+            assert p.last_config()["grid"] == 6
+
+
+def test_degenerate_shapes(plan):
+    A = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(32, 64, dtype=torch.bfloat16, device="cuda")
+    assert plan.gemm(A, B).shape == (0, 32)
+    n_before = plan.launch_count()
+    A = torch.ones(48, 0, dtype=torch.bfloat16, device="cuda")
+    B = torch.ones(40, 0, dtype=torch.bfloat16, device="cuda")
+    C = torch.full((48, 40), 3.0, dtype=torch.bfloat16, device="cuda")
+    plan.gemm(A, B, out=C)  # K = 0: the empty sum
+    assert plan.status() == 0
+    assert torch.all(C == 0)
+    assert plan.launch_count() == n_before  # no GEMM kernel for empty work
+
+
+def test_rejects_misaligned_on_device(plan):
+    A = torch.zeros(64, 72, dtype=torch.bfloat16, device="cuda")[:, 1:]  # base not 16 B aligned
+    B = torch.zeros(64, 71, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.BwgemmError) as e:
+        plan.gemm(A, B)
+    assert e.value.status == 2
+
+
+def test_host_buffers_round_trip(plan):
+    A = make_matrix(300, 264, "int2", seed=930)
+    B = make_matrix(200, 264, "int2", seed=931)
+    C = plan.gemm_host(A.pin_memory(), B.pin_memory())
+    ref = oracle.gemm(bits_of(A), bits_of(B), "bf16")
+    compare(bits_of(C), ref, "bf16", 264, exact=True)
+
+
+# ------------------------------------------------------- the pages' full shapes
+FULL = ["square4096", "square4096_fp16", "prefill_attn_out", "prefill_mlp_up",
+        "decode_attn_out", "decode_qkv", "decode_mlp_up", "decode_mlp_down",
+        "gemma_512x8192x5376", "tail_m1", "tail_m16", "tail_m64", "tail_m200"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_shape_sampled(plan, name):
+    s = SHAPES[name]
+    A, B = make_inputs(s, device="cuda")
+    C = plan.gemm(A, B)
+    assert plan.status() == 0
+    rows = sample_indices(s.M, 64, seed=1)
+    cols = sample_indices(s.N, 64, seed=2)
+    a_bits, b_bits = bits_of(A), bits_of(B)
+    c_rows = bits_of(C[torch.from_numpy(rows).cuda()])
+    c_cols = bits_of(C[:, torch.from_numpy(cols).cuda()])
+    ref_rows = oracle.gemm(a_bits, b_bits, s.dtype, rows=rows)
+    ref_cols = oracle.gemm(a_bits, b_bits, s.dtype, cols=cols)
+    compare(c_rows, ref_rows, s.dtype, s.K)
+    compare(c_cols, ref_cols, s.dtype, s.K)
+
+
+def test_full_square_integers_bit_exact(plan):
+    # 4096^3 with integer entries: every partial sum is an exact integer in fp32
+    s = SHAPES["square512_int"]
+    A = make_matrix(4096, 4096, "int2", seed=940, device="cuda")
+    B = make_matrix(4096, 4096, "int2", seed=941, device="cuda")
+    C = plan.gemm(A, B)
+    assert plan.status() == 0
+    rows = sample_indices(4096, 64, seed=3)
+    ref = oracle.gemm(bits_of(A), bits_of(B), "bf16", rows=rows)
+    compare(bits_of(C[torch.from_numpy(rows).cuda()]), ref, "bf16", 4096, exact=True)
+    del s

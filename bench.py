@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the bwgemm hot path: dense C = A * B^T in bf16 on one GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+plan lookup + TMA descriptors on the host, then one launch of the
+persistent tcgen05 kernel (producer / MMA / epilogue, split-K where the shape
+asks for it).  The headline workload is the 4096^3 square GEMM with
+N(0,1)/sqrt(K) bf16 operands; the pages' Llama-3-70B prefill and decode
+linears, the fp16 square and the tail shapes are timed alongside and
+reported under "shapes".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
+steps bracketed by a barrier and a device synchronisation on both sides.
+Inputs rotate over enough copies that their total exceeds twice the L2
+(129 MB), so no step reads operands left in L2 by the step before.  With N > 1
+(torchrun) every rank runs an independent replica ("replicas only": the GEMM
+has no exchange step), the max time over ranks is taken and `value` counts
+the work of all ranks.
+
+``--impl reference`` times the CPU oracle (the plain fp64 triple loop) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM TFLOP/s + % of GB300 dense roofline (4096³, prefill, M=256 decode)"
+HEADLINE = "square4096"
+EXTRA_SHAPES = ["square4096_fp16", "prefill_attn_out", "prefill_mlp_up", "decode_attn_out",
+                "decode_qkv", "decode_mlp_up", "decode_mlp_down", "gemma_512x8192x5376",
+                "tail_m1", "tail_m16", "tail_m64", "tail_m200"]
+PAGES_4096_BF16 = 1772.9  # TFLOP/s, the Blackwell deep dive's final kernel, on B200
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "gemm_sm103.cu", "planner.cpp",
+                  "api.cpp", "internal.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_gemm_blackwell_03_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) >= 3 and line[0] == want and line[1] == workload:
+                return int(line[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "util": float(parts[4]) if parts[4] not in ("", "[N/A]") else 0.0,
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "power_cap": parts[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("power_cap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len([r for r in rows if r["util"] >= 50])}
+
+
+def input_sets(shape, device, l2_bytes, max_sets=4):
+    """Enough seeded copies of (A, B, C) that consecutive steps never find
+    their operands in L2."""
+    import torch
+    from dense_gemm_blackwell_03_gb300.workloads import make_inputs, TORCH_DTYPES
+    set_bytes = shape.algorithmic_bytes
+    n = 1 if set_bytes >= 2 * l2_bytes else min(max_sets, math.ceil(3 * l2_bytes / set_bytes))
+    sets = []
+    for i in range(max(n, 1)):
+        A, B = make_inputs(shape, device=device, seed=None if i == 0 else 7919 * i + 17)
+        C = torch.empty((shape.M, shape.N), dtype=TORCH_DTYPES[shape.dtype], device=device)
+        sets.append((A, B, C))
+    return sets
+
+
+def time_steps(fn, sets, steps, warmup, stream, barrier=None):
+    """Run fn(A, B, C) steps times back to back (rotating sets); return the
+    per-step event times (ms) and the bracketed total (ms)."""
+    import torch
+    for i in range(warmup):
+        fn(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_begin.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        fn(*sets[i % len(sets)])
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, t_begin.elapsed_time(t_end)
+
+
+def roofline_entry(shape, seconds, peaks):
+    """Bound, achieved and peak for one shape (the min(peak, AI x BW) roofline)."""
+    flops = shape.flops
+    nbytes = shape.algorithmic_bytes
+    ai = flops / nbytes
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tflops = flops / seconds / 1e12
+    gbs = nbytes / seconds / 1e9
+    attainable = min(peaks["bf16_tflops"], ai * peaks["hbm_gbs"] / 1e3)
+    if ai >= ridge:
+        return {"bound": "tensor", "achieved": round(tflops, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
+                "roofline_frac": round(tflops / attainable, 4), "ai_flop_per_byte": round(ai, 1)}
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "roofline_frac": round(tflops / attainable, 4),
+            "ai_flop_per_byte": round(ai, 1), "tflops": round(tflops, 1)}
+
+
+def cpu_baseline(shape, target_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of rows."""
+    import oracle
+    from dense_gemm_blackwell_03_gb300.workloads import bits_of, make_inputs
+    A, B = make_inputs(shape, device="cpu")
+    a, b = bits_of(A), bits_of(B)
+    threads = oracle.max_threads()
+    probe = min(shape.M, max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.gemm(a, b, shape.dtype, rows=list(range(probe)))
+    rate = probe / (time.perf_counter() - t0)
+    rows = int(min(shape.M, max(probe, rate * target_s)))
+    sel = list(range(0, shape.M, max(1, shape.M // rows)))[:rows]
+    t0 = time.perf_counter()
+    oracle.gemm(a, b, shape.dtype, rows=sel)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * len(sel) * shape.N * shape.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{len(sel)} of {shape.M} rows of C ({len(sel)}x{shape.N}x{shape.K}, "
+                      f"fp64 triple loop, {dt:.1f} s on {threads} threads); "
+                      f"TFLOP/s extrapolated per row to the full {shape.M}x{shape.N}x{shape.K}"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed step by step on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_gemm_blackwell_03_gb300.workloads import SHAPES, bits_of, make_inputs
+    shape = SHAPES[args.shape]
+    A, B = make_inputs(shape, device="cpu")
+    a, b = bits_of(A), bits_of(B)
+    threads = oracle.max_threads()
+    # size each step so that warm-up + timed steps take about args.ref_budget seconds
+    t0 = time.perf_counter()
+    oracle.gemm(a, b, shape.dtype, rows=list(range(min(shape.M, threads))))
+    per_output = (time.perf_counter() - t0) / (min(shape.M, threads) * shape.N)
+    outputs = max(threads, int(args.ref_budget / (args.steps + args.warmup) / per_output))
+    # rows spread over all threads (the oracle parallelises over rows of C)
+    if outputs >= threads * shape.N:
+        nrows, ncols = min(shape.M, outputs // shape.N), None
+    else:
+        nrows = min(shape.M, threads)
+        ncols = list(range(max(1, min(shape.N, outputs // nrows))))
+    rows = list(range(nrows))
+    for _ in range(args.warmup):
+        oracle.gemm(a, b, shape.dtype, rows=rows, cols=ncols)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(a, b, shape.dtype, rows=rows, cols=ncols)
+        times.append(time.perf_counter() - t0)
+    n_out = nrows * (len(ncols) if ncols else shape.N)
+    flops = 2.0 * n_out * shape.K
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    sample = (f"{n_out} outputs of C per step ({nrows} row(s) x "
+              f"{len(ncols) if ncols else shape.N} cols, K={shape.K}), fp64 triple loop")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{shape.name}: C=A*B^T, M={shape.M} N={shape.N} K={shape.K}, "
+                               f"{shape.dtype} in/out", "M": shape.M, "N": shape.N, "K": shape.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from dense_gemm_blackwell_03_gb300 import binding
+    from dense_gemm_blackwell_03_gb300.workloads import SHAPES, TORCH_DTYPES, make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    barrier = (lambda: dist.barrier()) if dist else None
+
+    binding.load_library(build_if_missing=True)
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2_bytes = int(getattr(props, "L2_cache_size", 129 * 10 ** 6)) or 129 * 10 ** 6
+    shape = SHAPES[args.shape]
+    stream = torch.cuda.current_stream(device)
+    plan = binding.Plan(local_rank)
+
+    def ours(A, B, C):
+        plan.gemm(A, B, out=C, stream=stream)
+
+    sets = input_sets(shape, device, l2_bytes)
+    n0 = plan.launch_count()
+    sampler = ClockSampler(local_rank)
+    for i in range(args.warmup):
+        ours(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    launches_warm = plan.launch_count() - n0
+    sampler.start()
+    time.sleep(0.2)
+    per, total_ms = time_steps(ours, sets, args.steps, 0, stream, barrier)
+    clocks = sampler.stop()
+    launches = plan.launch_count() - n0 - launches_warm
+    st = plan.status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {st} after the timed region")
+    kcfg = plan.last_config()
+
+    total_s = total_ms / 1e3
+    if dist:
+        t = torch.tensor([total_s], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    ms_per_step = total_s * 1e3 / args.steps
+    value = world * shape.flops * args.steps / total_s / 1e12
+    per_sorted = sorted(per)
+    median_ms = statistics.median(per)
+    avg_launch_s = sum(per) / len(per) / 1e3
+
+    roof = roofline_entry(shape, avg_launch_s, peaks)
+    roofline = {"bound": roof["bound"], "achieved": roof["achieved"], "peak": roof["peak"],
+                "unit": roof["unit"], "frac": roof["frac"],
+                "traffic": recorded_traffic(shape.name),
+                "peak_source": f"{peaks['source']} ({'burst cuBLAS bf16' if roof['bound'] == 'tensor' else 'copy bandwidth'})",
+                "kernel": "bwgemm::gemm_kernel (persistent tcgen05)",
+                "algorithmic": (f"{shape.flops / 1e9:.1f} GFLOP per launch (2MNK)"
+                                if roof["bound"] == "tensor" else
+                                f"{shape.algorithmic_bytes / 1e6:.1f} MB per launch")}
+
+    # cuBLAS (torch.matmul) on the same tensors, as same-box context
+    def cublas(A, B, C):
+        torch.matmul(A, B.t(), out=C)
+    per_cb, _ = time_steps(cublas, sets, min(args.steps, 200), 5, stream, barrier)
+
+    # end-to-end through the C ABI with host buffers (H2D of A, B and D2H of C each step)
+    e2e = None
+    if not args.no_e2e:
+        A0, B0, _ = sets[0]
+        hA = A0.cpu().pin_memory()
+        hB = B0.cpu().pin_memory()
+        hC = torch.empty((shape.M, shape.N), dtype=TORCH_DTYPES[shape.dtype]).pin_memory()
+        for _ in range(3):
+            plan.gemm_host(hA, hB, out=hC, stream=stream)
+        e2e_steps = max(5, min(args.steps, 30))
+        if barrier:
+            barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            plan.gemm_host(hA, hB, out=hC, stream=stream)
+        e2e_s = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([e2e_s], device=device, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": round(world * shape.flops * e2e_steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 2 * (shape.M * shape.K + shape.N * shape.K),
+               "d2h_bytes_per_step": 2 * shape.M * shape.N, "steps": e2e_steps,
+               "api": "bwgemm_run_host (pinned host A, B, C)"}
+
+    # the pages' other shapes, timed alongside (not the headline)
+    shapes = {}
+    if not args.no_extra:
+        for name in EXTRA_SHAPES:
+            s = SHAPES[name]
+            ssets = input_sets(s, device, l2_bytes, max_sets=3)
+            it = 50
+            p_ours, _ = time_steps(ours, ssets, it, 5, stream)
+            if plan.status(stream) != 0:
+                raise SystemExit(f"device status error on {name}")
+            cfg = plan.last_config()
+            p_cb, _ = time_steps(cublas, ssets, it, 5, stream)
+            t = statistics.median(p_ours) / 1e3
+            r = roofline_entry(s, t, peaks)
+            shapes[name] = {"M": s.M, "N": s.N, "K": s.K, "dtype": s.dtype,
+                            "median_us": round(t * 1e6, 2),
+                            "tflops": round(s.flops / t / 1e12, 1),
+                            "gbs": round(s.algorithmic_bytes / t / 1e9, 1),
+                            "roofline": r,
+                            "cublas_tflops": round(s.flops / (statistics.median(p_cb) / 1e3) / 1e12, 1),
+                            "kernel_config": {k: cfg[k] for k in ("variant", "tile_m", "tile_n",
+                                                                  "split_k", "grid")}}
+            del ssets
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, target_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": round(value / world / PAGES_4096_BF16, 4),
+            "vs_baseline_ref": "1772.9 TFLOP/s bf16 4096^3 on B200 (the Blackwell deep dive's "
+                               "kernel 8); another machine's number, context only",
+            "dtype": shape.dtype,
+            "data": "synthetic: seeded N(0,1)/sqrt(K) bf16 A and B, rounded from fp32",
+            "config": {"workload": f"{shape.name}: C=A*B^T, M={shape.M} N={shape.N} K={shape.K}, "
+                                   f"{shape.dtype} in/out, fp32 accumulate",
+                       "M": shape.M, "N": shape.N, "K": shape.K,
+                       "l2": f"inputs rotate over {len(sets)} copies "
+                             f"({len(sets) * shape.algorithmic_bytes / 1e6:.0f} MB > 2x L2)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "kernel_config": kcfg},
+            "median_ms": round(median_ms, 5),
+            "p10_ms": round(per_sorted[len(per) // 10], 5),
+            "p90_ms": round(per_sorted[(9 * len(per)) // 10], 5),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "cublas_tflops": round(shape.flops / (statistics.median(per_cb) / 1e3) / 1e12, 1),
+            "peaks": peaks,
+            "shapes": shapes,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--shape", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="skip the pages' other shapes")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="seconds of oracle work for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

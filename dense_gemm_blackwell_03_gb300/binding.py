@@ -30,7 +30,7 @@ EXPORTED = [
     "bwgemm_default_options", "bwgemm_create_plan", "bwgemm_destroy", "bwgemm_run",
     "bwgemm_run_host", "bwgemm_get_status", "bwgemm_last_device_status", "bwgemm_check_args",
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
-    "bwgemm_status_string", "bwgemm_version",
+    "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
 ]
 
 
@@ -111,6 +111,9 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_run.restype = st
         lib.bwgemm_run_host.argtypes = gemm_args
         lib.bwgemm_run_host.restype = st
+        lib.bwgemm_run_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                                  ctypes.c_int, i32, vp]
+        lib.bwgemm_run_splitk_noalloc.restype = st
         lib.bwgemm_get_status.argtypes = [vp, vp]
         lib.bwgemm_get_status.restype = st
         lib.bwgemm_last_device_status.argtypes = [vp]

@@ -176,6 +176,41 @@ bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out
 /* Number of GEMM kernels the plan has enqueued since it was created. */
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);
 
+/*
+ * C = A * B^T with split-K, allocating no device memory (the source pages
+ * have no counterpart to this entry point).
+ *
+ * For callers that cannot call cudaMalloc -- code running under a memory
+ * manager that has already reserved the device's memory, code whose device
+ * footprint must stay fixed after start-up, or loops that must not risk the
+ * device-wide synchronisation cudaMalloc / cudaFree can cause -- and so
+ * cannot create a plan.  Needs no plan: the split-K scratch (fp32 partial
+ * tiles, arrival counters, a status word) lives in one fixed device array of
+ * 8 MiB + 64 KiB + 256 B inside the library, present on every GPU that loads
+ * it until the process exits.
+ *
+ *   A, B, C, M, N, K, lda, ldb, ldc, dtype : as for bwgemm_run (caller-owned
+ *          device pointers; same alignment rules and error codes)
+ *   split_k : K slices per output tile, 2..16 (capped at the number of
+ *          64-wide K blocks); the partial tiles of all slices must fit the
+ *          8 MiB array (tiles x split_k x 128 KiB for the 256-column tiles),
+ *          else BWGEMM_ERR_WORKSPACE is returned and nothing is launched
+ *   stream : cudaStream_t (NULL = legacy default stream)
+ *
+ * The first call on a device (with that device current) resolves the
+ * array's device address and occupancy limits; make that first call before
+ * any stream capture.  Every call shares the array, which keeps the previous
+ * call's contents; each call clears the counters and status word it uses on
+ * `stream` first.  Calls whose kernels may overlap on the GPU (other streams,
+ * other host threads) race on the array: serialise them.  Device-side wait
+ * timeouts of this entry point are not reported (there is no plan to hold
+ * the status); use the plan API when that matters.
+ */
+bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* B, void* C, int64_t M,
+                                          int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                          int64_t ldc, bwgemm_dtype_t dtype, int32_t split_k,
+                                          void* stream);
+
 /* Static text for a status code ("unknown status" for anything else). */
 const char* bwgemm_status_string(bwgemm_status_t status);
 

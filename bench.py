@@ -158,31 +158,41 @@ def input_sets(shape, device, l2_bytes, max_sets=4):
     return sets
 
 
-def time_steps(fn, sets, steps, warmup, stream, barrier=None):
-    """Run fn(A, B, C) steps times back to back (rotating sets); return the
-    per-step event times (ms) and the bracketed total (ms)."""
+def time_region(fn, sets, steps, warmup, stream, barrier=None):
+    """Run fn(A, B, C) `steps` times back to back (rotating input sets) between
+    two events on the launching stream, bracketed by a barrier and a device
+    synchronisation on both sides; return the elapsed milliseconds."""
     import torch
     for i in range(warmup):
         fn(*sets[i % len(sets)])
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
     t_begin.record(stream)
     for i in range(steps):
-        starts[i].record(stream)
         fn(*sets[i % len(sets)])
-        ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return per, t_begin.elapsed_time(t_end)
+    return t_begin.elapsed_time(t_end)
+
+
+def time_each(fn, sets, iters, stream):
+    """Per-iteration event times (ms) for the median / percentiles: each
+    iteration is bracketed by its own pair of events."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for i in range(iters):
+        starts[i].record(stream)
+        fn(*sets[i % len(sets)])
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
 def roofline_entry(shape, seconds, peaks):
@@ -308,21 +318,21 @@ def run_ours(args):
         plan.gemm(A, B, out=C, stream=stream)
 
     sets = input_sets(shape, device, l2_bytes)
-    n0 = plan.launch_count()
-    sampler = ClockSampler(local_rank)
     for i in range(args.warmup):
         ours(*sets[i % len(sets)])
     torch.cuda.synchronize()
-    launches_warm = plan.launch_count() - n0
+    n0 = plan.launch_count()
+    sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.2)
-    per, total_ms = time_steps(ours, sets, args.steps, 0, stream, barrier)
+    total_ms = time_region(ours, sets, args.steps, 0, stream, barrier)
     clocks = sampler.stop()
-    launches = plan.launch_count() - n0 - launches_warm
+    launches = plan.launch_count() - n0
     st = plan.status(stream)
     if st != 0:
         raise SystemExit(f"device status {st} after the timed region")
     kcfg = plan.last_config()
+    per = time_each(ours, sets, max(50, min(args.steps, 200)), stream)
 
     total_s = total_ms / 1e3
     if dist:
@@ -333,7 +343,7 @@ def run_ours(args):
     value = world * shape.flops * args.steps / total_s / 1e12
     per_sorted = sorted(per)
     median_ms = statistics.median(per)
-    avg_launch_s = sum(per) / len(per) / 1e3
+    avg_launch_s = total_s / args.steps  # one kernel launch per step, back to back
 
     roof = roofline_entry(shape, avg_launch_s, peaks)
     roofline = {"bound": roof["bound"], "achieved": roof["achieved"], "peak": roof["peak"],
@@ -348,7 +358,8 @@ def run_ours(args):
     # cuBLAS (torch.matmul) on the same tensors, as same-box context
     def cublas(A, B, C):
         torch.matmul(A, B.t(), out=C)
-    per_cb, _ = time_steps(cublas, sets, min(args.steps, 200), 5, stream, barrier)
+    cb_ms = time_region(cublas, sets, min(args.steps, 300), 5, stream, barrier)
+    cb_s = cb_ms / 1e3 / min(args.steps, 300)
 
     # end-to-end through the C ABI with host buffers (H2D of A, B and D2H of C each step)
     e2e = None
@@ -381,22 +392,22 @@ def run_ours(args):
         for name in EXTRA_SHAPES:
             s = SHAPES[name]
             ssets = input_sets(s, device, l2_bytes, max_sets=3)
-            it = 50
-            p_ours, _ = time_steps(ours, ssets, it, 5, stream)
+            it = 100
+            t = time_region(ours, ssets, it, 5, stream) / 1e3 / it
             if plan.status(stream) != 0:
                 raise SystemExit(f"device status error on {name}")
             cfg = plan.last_config()
-            p_cb, _ = time_steps(cublas, ssets, it, 5, stream)
-            t = statistics.median(p_ours) / 1e3
+            med = statistics.median(time_each(ours, ssets, 50, stream)) / 1e3
+            t_cb = time_region(cublas, ssets, it, 5, stream) / 1e3 / it
             r = roofline_entry(s, t, peaks)
             shapes[name] = {"M": s.M, "N": s.N, "K": s.K, "dtype": s.dtype,
-                            "median_us": round(t * 1e6, 2),
+                            "us": round(t * 1e6, 2), "median_us": round(med * 1e6, 2),
                             "tflops": round(s.flops / t / 1e12, 1),
                             "gbs": round(s.algorithmic_bytes / t / 1e9, 1),
                             "roofline": r,
-                            "cublas_tflops": round(s.flops / (statistics.median(p_cb) / 1e3) / 1e12, 1),
+                            "cublas_tflops": round(s.flops / t_cb / 1e12, 1),
                             "kernel_config": {k: cfg[k] for k in ("variant", "tile_m", "tile_n",
-                                                                  "split_k", "grid")}}
+                                                                  "split_k", "schedule", "grid")}}
             del ssets
             torch.cuda.empty_cache()
 
@@ -430,12 +441,13 @@ def run_ours(args):
             "median_ms": round(median_ms, 5),
             "p10_ms": round(per_sorted[len(per) // 10], 5),
             "p90_ms": round(per_sorted[(9 * len(per)) // 10], 5),
+            "per_iteration_note": f"median/p10/p90 over {len(per)} separately event-timed iterations",
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,
-            "cublas_tflops": round(shape.flops / (statistics.median(per_cb) / 1e3) / 1e12, 1),
+            "cublas_tflops": round(shape.flops / cb_s / 1e12, 1),
             "peaks": peaks,
             "shapes": shapes,
         }

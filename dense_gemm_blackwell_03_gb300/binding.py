@@ -14,6 +14,10 @@ import threading
 BF16 = 0
 FP16 = 1
 
+SCHEDULE_AUTO = 0
+SCHEDULE_TILES = 1
+SCHEDULE_STREAM_K = 2
+
 STATUS_NAMES = {
     0: "BWGEMM_OK",
     1: "BWGEMM_ERR_INVALID_ARG",
@@ -31,7 +35,13 @@ EXPORTED = [
     "bwgemm_run_host", "bwgemm_get_status", "bwgemm_last_device_status", "bwgemm_check_args",
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
     "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
+    "bwgemm_plan_read_trace",
 ]
+
+# timeline slots of bwgemm_plan_read_trace
+TRACE_ENTRY, TRACE_READY, TRACE_FIRST_LOAD, TRACE_LAST_LOAD, TRACE_EPI_DONE, TRACE_EXIT = range(6)
+TRACE_UNIT0 = 8
+TRACE_UNITS = 14
 
 
 class BwgemmError(RuntimeError):
@@ -51,7 +61,11 @@ class PlanOptions(ctypes.Structure):
         ("stall_kblock", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64),
         ("workspace_bytes", ctypes.c_uint64),
-        ("reserved", ctypes.c_int32 * 8),
+        ("schedule", ctypes.c_int32),
+        ("pdl_off", ctypes.c_int32),
+        ("trace", ctypes.c_int32),
+        ("prefetch", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -68,6 +82,12 @@ class Config(ctypes.Structure):
         ("num_units", ctypes.c_int32),
         ("grid", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
+        ("schedule", ctypes.c_int32),
+        ("dp_tiles", ctypes.c_int32),
+        ("sk_tiles", ctypes.c_int32),
+        ("workers", ctypes.c_int32),
+        ("split_scatter", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -125,6 +145,9 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_select_config.restype = st
         lib.bwgemm_plan_last_config.argtypes = [vp, ctypes.POINTER(Config)]
         lib.bwgemm_plan_last_config.restype = st
+        lib.bwgemm_plan_read_trace.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), i64,
+                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.bwgemm_plan_read_trace.restype = st
         lib.bwgemm_plan_launch_count.argtypes = [vp]
         lib.bwgemm_plan_launch_count.restype = ctypes.c_uint64
         lib.bwgemm_status_string.argtypes = [ctypes.c_int]
@@ -280,6 +303,20 @@ class Plan:
 
     def launch_count(self) -> int:
         return int(self.lib.bwgemm_plan_launch_count(self.handle))
+
+    def read_trace(self):
+        """Timeline of the last launch (plan created with trace=1): a
+        (ctas, slots) numpy uint64 array of %globaltimer stamps in ns."""
+        import numpy as np
+        cap = 1 << 16
+        buf = (ctypes.c_uint64 * cap)()
+        ctas, slots = ctypes.c_int32(), ctypes.c_int32()
+        rc = self.lib.bwgemm_plan_read_trace(self.handle, buf, cap, ctypes.byref(ctas),
+                                             ctypes.byref(slots))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_plan_read_trace")
+        n = ctas.value * slots.value
+        return np.ctypeslib.as_array(buf)[:n].copy().reshape(ctas.value, slots.value)
 
 
 _plans: dict = {}

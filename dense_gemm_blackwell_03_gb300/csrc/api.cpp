@@ -118,6 +118,10 @@ struct bwgemm_plan_s {
     // device staging buffers of bwgemm_run_host
     void* h2d[3] = {nullptr, nullptr, nullptr};
     size_t h2d_cap[3] = {0, 0, 0};
+    // optional timeline (opts.trace): kTraceSlots stamps per CTA of the last launch
+    uint64_t* d_trace = nullptr;
+    int trace_ctas = 0;
+    int last_grid = 0;
 };
 
 namespace {
@@ -153,31 +157,30 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
                        CU_TENSOR_MAP_SWIZZLE_64B)) != BWGEMM_OK)
         return st;
 
-    GemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.M = int32_t(M);
-    p.N = int32_t(N);
-    p.K = int32_t(K);
-    p.num_m_blocks = sel.num_m_blocks;
-    p.num_n_blocks = sel.num_n_blocks;
-    p.num_k_blocks = sel.num_k_blocks;
-    p.num_tiles = sel.cfg.num_tiles;
-    p.split_k = sel.cfg.split_k;
-    p.num_units = sel.cfg.num_units;
-    p.raster_group = sel.cfg.raster_group;
-    p.dtype = int32_t(dtype);
-    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
+    GemmParams p = make_params(sel, M, N, K, dtype);
     p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
     p.status = plan->d_status;
     p.tile_sems = reinterpret_cast<uint32_t*>(plan->d_workspace);
     p.partials = reinterpret_cast<float*>(plan->d_workspace + kCounterRegionBytes);
     p.stall_kblock = plan->opts.stall_kblock;
+    if (plan->opts.prefetch != 0)
+        p.prefetch = plan->opts.prefetch < 0 ? 0 : plan->opts.prefetch;
+    if (plan->d_trace) {
+        if (sel.cfg.grid > plan->trace_ctas)
+            return BWGEMM_ERR_UNSUPPORTED;
+        if (cudaMemsetAsync(plan->d_trace, 0, size_t(sel.cfg.grid) * kTraceSlots * sizeof(uint64_t),
+                            stream) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+        p.trace = plan->d_trace;
+    }
 
     const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
-                                           plan->tmaps[2].map, p, sel.cfg.grid, stream);
+                                           plan->tmaps[2].map, p, sel.cfg.grid, stream,
+                                           plan->opts.pdl_off == 0);
     if (err != cudaSuccess)
         return BWGEMM_ERR_CUDA;
     plan->last = sel.cfg;
+    plan->last_grid = sel.cfg.grid;
     plan->launches += 1;
     return BWGEMM_OK;
 }
@@ -259,6 +262,15 @@ bwgemm_status_t bwgemm_create_plan(bwgemm_plan_t* out, int device,
         delete plan;
         return BWGEMM_ERR_CUDA;
     }
+    if (o.trace) {
+        plan->trace_ctas = sms;
+        if (cudaMalloc(&plan->d_trace, size_t(sms) * kTraceSlots * sizeof(uint64_t)) != cudaSuccess) {
+            cudaFree(plan->d_status);
+            cudaFree(plan->d_workspace);
+            delete plan;
+            return BWGEMM_ERR_CUDA;
+        }
+    }
     *out = plan;
     return BWGEMM_OK;
 }
@@ -271,6 +283,8 @@ bwgemm_status_t bwgemm_destroy(bwgemm_plan_t plan)
     cudaDeviceSynchronize();
     cudaFree(plan->d_status);
     cudaFree(plan->d_workspace);
+    if (plan->d_trace)
+        cudaFree(plan->d_trace);
     for (void* b : plan->h2d)
         if (b)
             cudaFree(b);
@@ -367,5 +381,23 @@ bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out
 }
 
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan) { return plan ? plan->launches : 0u; }
+
+bwgemm_status_t bwgemm_plan_read_trace(bwgemm_plan_t plan, uint64_t* out, int64_t capacity,
+                                       int32_t* ctas, int32_t* slots)
+{
+    if (!plan || !plan->d_trace || !out || !ctas || !slots)
+        return BWGEMM_ERR_INVALID_ARG;
+    const int64_t n = int64_t(plan->last_grid) * kTraceSlots;
+    if (capacity < n)
+        return BWGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(out, plan->d_trace, size_t(n) * sizeof(uint64_t), cudaMemcpyDeviceToHost) !=
+            cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    *ctas = plan->last_grid;
+    *slots = kTraceSlots;
+    return BWGEMM_OK;
+}
 
 }  // extern "C"

@@ -8,13 +8,16 @@
 //               and B (128B-swizzled), guarded by full/empty mbarrier pairs.
 //   warp 1      TMEM allocator; lane 0 (of the leader CTA) issues every
 //               tcgen05.mma and commits stage release / accumulator-ready.
-//   warps 2..5  epilogue: tcgen05.ld -> fp32 -> bf16/fp16 -> swizzled smem ->
-//               TMA store, double-buffered per warp; with split-K, every
-//               split writes an fp32 partial and the last to arrive sums
-//               them in split order and stores C.
+//   warps 2..9  epilogue (two per TMEM lane quarter, half the columns each):
+//               tcgen05.ld -> fp32 -> bf16/fp16 -> swizzled smem -> TMA store,
+//               double-buffered per warp.  A unit that covers only part of a
+//               tile's K range (split-K slice or stream-K piece) combines
+//               with the tile's other pieces through fp32 partials in a
+//               fixed order (see the epilogue), without waiting on them.
 // Two fp32 accumulators live in TMEM (2 x BN columns), so the epilogue of one
-// work unit overlaps the MMAs of the next.  Work units (tile, k-split) are
-// handed out statically in a grouped raster order.
+// work unit overlaps the MMAs of the next.  Work is handed out statically:
+// each worker (CTA or CTA pair) first walks its share of the stream-K
+// iterations, then its data-parallel tiles, in grouped raster order.
 //
 // Where the pages describe each part:
 //   ring + phase tracking, producer/consumer warps, empty barriers passing on
@@ -64,7 +67,7 @@ struct KernelConfig {
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KiB
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
     static_assert(kSmemBytes <= 227 * 1024, "exceeds the 227 KiB shared memory of one CTA");
-    // bytes of one CTA's fp32 partial tile (split-K)
+    // floats of one CTA's fp32 partial tile
     static constexpr int kPartialFloats = kRowsPerCta * BN;
 };
 
@@ -84,30 +87,103 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t smem)
     return d;
 }
 
+enum : int { kUnitWhole = 0, kUnitSplit = 1, kUnitStreamK = 2 };
+
 struct WorkUnit {
-    int tile, split;
+    int tile;      // raster tile id
     int m_blk, n_blk;
     int kb0, kb1;  // K blocks [kb0, kb1)
+    int kind;      // kUnitWhole / kUnitSplit / kUnitStreamK
+    int split;     // split-K slice index
+    int sk_tile;   // stream-K tile index within the stream-K region
+    int slot;      // stream-K: 0 = first unit of this worker's range, 1 = its last
 };
 
-__device__ __forceinline__ WorkUnit decode_unit(const GemmParams& p, int u)
+// Grouped raster: walk `raster_group` m-blocks down, then step along N.
+__device__ __forceinline__ void raster(const GemmParams& p, int tile, int& m_blk, int& n_blk)
 {
-    WorkUnit w;
-    const int S = p.split_k;
-    w.tile = u / S;
-    w.split = u - w.tile * S;
-    w.kb0 = int((long long)w.split * p.num_k_blocks / S);
-    w.kb1 = int((long long)(w.split + 1) * p.num_k_blocks / S);
-    // grouped raster: walk `raster_group` m-blocks down, then step along N
     const int G = p.raster_group;
     const int per_group = G * p.num_n_blocks;
-    const int g = w.tile / per_group;
+    const int g = tile / per_group;
     const int first_m = g * G;
     const int gm = min(p.num_m_blocks - first_m, G);
-    const int local = w.tile - g * per_group;
-    w.m_blk = first_m + local % gm;
-    w.n_blk = local / gm;
-    return w;
+    const int local = tile - g * per_group;
+    m_blk = first_m + local % gm;
+    n_blk = local / gm;
+}
+
+// First stream-K iteration of `worker` (of `workers`).
+__device__ __forceinline__ long long sk_begin(const GemmParams& p, int worker, int workers)
+{
+    return (long long)worker * p.sk_iters / workers;
+}
+
+// The worker whose stream-K range holds iteration `it`.
+__device__ __forceinline__ int sk_owner(const GemmParams& p, long long it, int workers)
+{
+    return int(((it + 1) * workers - 1) / p.sk_iters);
+}
+
+// The sequence of work units of one worker; every role walks the same one.
+struct UnitIter {
+    long long it, it_begin, it_end;  // this worker's stream-K iterations
+    int u, u_end, step;              // data-parallel units u, u + step, ...
+
+    __device__ __forceinline__ void init(const GemmParams& p, int worker, int workers)
+    {
+        it_begin = sk_begin(p, worker, workers);
+        it_end = sk_begin(p, worker + 1, workers);
+        it = it_begin;
+        u = worker;
+        u_end = p.dp_units;
+        step = workers;
+    }
+
+    __device__ __forceinline__ bool next(const GemmParams& p, WorkUnit& w)
+    {
+        if (it < it_end) {
+            const int KB = p.num_k_blocks;
+            const int t = int(it / KB);
+            w.kb0 = int(it - (long long)t * KB);
+            w.kb1 = int(min((long long)KB, (long long)w.kb0 + (it_end - it)));
+            w.kind = (w.kb0 == 0 && w.kb1 == KB) ? kUnitWhole : kUnitStreamK;
+            w.sk_tile = t;
+            w.slot = (it == it_begin) ? 0 : 1;
+            w.split = 0;
+            w.tile = p.dp_tiles + t;
+            it += w.kb1 - w.kb0;
+        } else if (u < u_end) {
+            // slices of a tile in reverse K order: slice 0, the one that waits
+            // for the others, has the largest unit id of its tile, so every
+            // slice it waits for comes earlier in every worker's sequence
+            const int S = p.split_k;
+            w.tile = u / S;
+            w.split = S - 1 - (u - w.tile * S);
+            w.kb0 = int((long long)w.split * p.num_k_blocks / S);
+            w.kb1 = int((long long)(w.split + 1) * p.num_k_blocks / S);
+            w.kind = (S > 1) ? kUnitSplit : kUnitWhole;
+            w.sk_tile = 0;
+            w.slot = 0;
+            u += step;
+        } else {
+            return false;
+        }
+        raster(p, w.tile, w.m_blk, w.n_blk);
+        return true;
+    }
+};
+
+__device__ __forceinline__ void trace_mark(const GemmParams& p, int slot)
+{
+    if (p.trace)
+        p.trace[size_t(blockIdx.x) * kTraceSlots + slot] = ptx::global_timer_ns();
+}
+
+__device__ __forceinline__ void trace_unit(const GemmParams& p, int unit, int which)
+{
+    if (p.trace && unit < kTraceUnits)
+        p.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnit0 + 4 * unit + which] =
+            ptx::global_timer_ns();
 }
 
 // Bounded wait on an mbarrier phase.  Gives up after p.timeout_ns (recording
@@ -126,6 +202,52 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
             return false;
         if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
             atomicOr(p.status, code);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+// Bounded wait until a global counter reaches `want` (written by other CTAs
+// with release semantics).  Gives up like wait_phase.
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t want, const GemmParams& p,
+                                             volatile uint32_t* abort_flag)
+{
+    if (ptx::ld_acquire_gpu(ctr) == want)
+        return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(64);
+        if (ptx::ld_acquire_gpu(ctr) == want)
+            return true;
+        if (*abort_flag)
+            return false;
+        if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kStatusSplitTimeout);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+// Bounded wait until a global counter reaches at least `want`.
+__device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint32_t want,
+                                                      const GemmParams& p,
+                                                      volatile uint32_t* abort_flag)
+{
+    if (ptx::ld_acquire_gpu(ctr) >= want)
+        return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(32);
+        if (ptx::ld_acquire_gpu(ctr) >= want)
+            return true;
+        if (*abort_flag)
+            return false;
+        if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kStatusSplitTimeout);
             *abort_flag = 1u;
             return false;
         }
@@ -205,27 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-    const int cluster_id = blockIdx.x / CG;
-    const int num_clusters = gridDim.x / CG;
+    const int worker = blockIdx.x / CG;
+    const int workers = gridDim.x / CG;
 
     const uint32_t sA = base + Cfg::kOffA;
     const uint32_t sB = base + Cfg::kOffB;
     const uint32_t sStore = base + Cfg::kOffStore;
-    const uint32_t bar_full = base + Cfg::kOffBar;      // + 8 * stage
-    const uint32_t bar_empty = bar_full + 8 * STAGES;   // + 8 * stage
+    const uint32_t bar_full = base + Cfg::kOffBar;         // + 8 * stage
+    const uint32_t bar_empty = bar_full + 8 * STAGES;      // + 8 * stage
     const uint32_t bar_acc_full = bar_empty + 8 * STAGES;  // + 8 * buffer
     const uint32_t bar_acc_empty = bar_acc_full + 16;      // + 8 * buffer
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
 
     if (threadIdx.x == 0) {
+        trace_mark(p, kTraceEntry);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);   // producer's arrive.expect_tx (+ bytes)
             ptx::mbar_init(bar_empty + 8 * s, 1);  // one tcgen05.commit
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar_acc_full + 8 * b, 1);                 // one tcgen05.commit
-            ptx::mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);   // every epilogue warp of the pair
+            ptx::mbar_init(bar_acc_full + 8 * b, 1);                // one tcgen05.commit
+            ptx::mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);  // every epilogue warp of the pair
         }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -247,25 +370,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Everything above may overlap the previous kernel on the stream
+    // (programmatic dependent launch); nothing below touches global memory
+    // before that kernel has completed.  Then let the next kernel be scheduled.
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    if (threadIdx.x == 0)
+        trace_mark(p, kTraceReady);
+
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-                const WorkUnit w = decode_unit(p, u);
+            bool first_unit = true;
+            UnitIter iter;
+            iter.init(p, worker, workers);
+            WorkUnit w;
+            while (ok && iter.next(p, w)) {
                 const int a_row = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta;
                 const int b_row = w.n_blk * BN + int(rank) * Cfg::kBRows;
+                // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
+                // ring only has to cover L2 latency, not DRAM latency
+                const int pf = p.prefetch;
+                for (int kb = w.kb0; kb < min(w.kb1, w.kb0 + pf); ++kb) {
+                    ptx::tma_prefetch_2d(&tmap_a, kb * kTileK, a_row);
+                    ptx::tma_prefetch_2d(&tmap_b, kb * kTileK, b_row);
+                }
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (pf > 0 && kb + pf < w.kb1) {
+                        ptx::tma_prefetch_2d(&tmap_a, (kb + pf) * kTileK, a_row);
+                        ptx::tma_prefetch_2d(&tmap_b, (kb + pf) * kTileK, b_row);
+                    }
                     if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, p, abort_flag,
                                     kStatusProducerTimeout)) {
                         ok = false;
                         break;
                     }
-                    const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 &&
-                                       u == cluster_id && kb - w.kb0 == p.stall_kblock;
+                    const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 && first_unit &&
+                                       kb - w.kb0 == p.stall_kblock;
                     if (!stall) {
+                        if (first_unit && kb == w.kb0)
+                            trace_mark(p, kTraceFirstLoad);
                         const uint32_t fb = bar_full + 8 * stage;
                         const uint32_t dA = sA + stage * Cfg::kABytes;
                         const uint32_t dB = sB + stage * Cfg::kBBytes;
@@ -287,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                first_unit = false;
             }
+            trace_mark(p, kTraceLastLoad);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
@@ -299,14 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int t = 0;
             bool ok = true;
-            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++t) {
-                const WorkUnit w = decode_unit(p, u);
+            UnitIter iter;
+            iter.init(p, worker, workers);
+            WorkUnit w;
+            while (ok && iter.next(p, w)) {
                 const int buf = t & 1;
                 const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
+                ++t;
                 if (!wait_phase(bar_acc_empty + 8 * buf, acc_phase ^ 1u, p, abort_flag,
                                 kStatusMmaTimeout))
                     break;
                 ptx::tc_fence_after_sync();
+                trace_unit(p, t - 1, 0);
                 const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(bar_full + 8 * stage, phase, p, abort_flag, kStatusMmaTimeout)) {
@@ -337,111 +490,309 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_commit(bar_acc_full + 8 * buf);
                 else
                     ptx::mma_commit_pair(bar_acc_full + 8 * buf, 0x3);
+                trace_unit(p, t - 1, 1);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // Warps 2..9: two per TMEM lane quarter q (= warp % 4, the quarter a
+        // warp may access); h selects the half of the columns it handles.
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const int h = ew >> 2;
+        constexpr int kChunks = BN / kStoreCols / 2;  // 32-column chunks per warp
+        const int c_begin = h * kChunks;
+        const int c_end = c_begin + kChunks;
         const int row = q * 32 + lane;
-        const uint32_t my_store = sStore + uint32_t((warp - 2) * 2 * Cfg::kStoreBufBytes);
+        const uint32_t my_store = sStore + uint32_t(ew * 2 * Cfg::kStoreBufBytes);
+        constexpr size_t kSlotF4 = size_t(Cfg::kPartialFloats) / 4;  // float4s per CTA partial
+        float4* const parts = reinterpret_cast<float4*>(p.partials);
         int chunk_ctr = 0;
         int t = 0;
-        for (int u = cluster_id; u < p.num_units; u += num_clusters, ++t) {
-            const WorkUnit w = decode_unit(p, u);
+        UnitIter iter;
+        iter.init(p, worker, workers);
+        WorkUnit w;
+        while (iter.next(p, w)) {
+            if (t > 0 && warp == 2 && lane == 0)
+                trace_unit(p, t - 1, 3);  // previous unit's epilogue finished
             const int buf = t & 1;
             const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
+            ++t;
             if (!wait_phase(bar_acc_full + 8 * buf, acc_phase, p, abort_flag,
                             kStatusEpilogueTimeout))
                 break;
             ptx::tc_fence_after_sync();
+            if (warp == 2 && lane == 0)
+                trace_unit(p, t - 1, 2);
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            const int m_row = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta + q * 32;
+            const int cta_row0 = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta;
+            const int m_row = cta_row0 + q * 32;  // first row of this warp's boxes
             const int n_col = w.n_blk * BN;
-            if (p.split_k == 1) {
-                // ---- direct epilogue: TMEM -> registers -> bf16/fp16 -> smem -> TMA store
+            if (m_row >= p.M) {
+                // every row of this warp is padding past M: nothing to load or store
+                // (the same holds for every piece of the tile, so no counter is used)
+                release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                continue;
+            }
+            if (w.kind == kUnitWhole) {
+                // ---- whole tile: TMEM -> registers -> bf16/fp16 -> smem -> TMA store
 #pragma unroll 1
-                for (int c = 0; c < BN / kStoreCols; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                     ptx::tmem_ld_wait();
-                    if (c == BN / kStoreCols - 1)
+                    if (c == c_end - 1)
                         release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
                     store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
                 }
-            } else {
-                // ---- split-K: every split stores its fp32 partial; the last of
-                // the S splits to arrive (per warp quarter) sums all S partials in
-                // split order 0..S-1 -- the same order whichever arrives last --
-                // and writes C.  No split waits on another.
+                continue;
+            }
+
+            if (w.kind == kUnitSplit && p.split_scatter) {
+                // ---- split-K, one wave: all S slices of the tile run at once, one
+                // per worker.  Chunk c of the tile belongs to slice c % S.  Each
+                // slice stores the chunks it does not own, counts itself, waits
+                // for the other S - 1 (bounded: they never wait on anything
+                // before storing), then sums its own chunks over slices 0..S-1 in
+                // order -- its own share straight from TMEM -- and stores C.
                 const int S = p.split_k;
+                const int j = w.split;
                 const int ctile = w.tile * CG + int(rank);
-                // partial slot layout per (tile, split, cta): [chunk][v = 0..7][row 0..127] float4
-                float4* slot0 = reinterpret_cast<float4*>(p.partials) +
-                                size_t(w.tile * S * CG + int(rank)) * (Cfg::kPartialFloats / 4);
-                const size_t split_stride = size_t(CG) * (Cfg::kPartialFloats / 4);
-                float4* mine = slot0 + size_t(w.split) * split_stride + row;
+                uint32_t* const cnt = p.tile_sems + size_t(ctile * kEpiWarps + ew) * kCountersPerWarp;
+                const bool row_ok = (cta_row0 + row) < p.M;
+                auto chunk_ptr = [&](int slice, int c) -> float4* {
+                    const size_t slot = size_t(w.tile * S + slice) * CG + rank;
+                    return parts + slot * kSlotF4 + size_t(c) * 8 * kRowsPerCta + row;
+                };
+                bool owns_any = false;
 #pragma unroll 1
-                for (int c = 0; c < BN / kStoreCols; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
+                    if (c % S == j) {
+                        owns_any = true;
+                        continue;
+                    }
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                     ptx::tmem_ld_wait();
-                    if (c == BN / kStoreCols - 1)
+                    if (row_ok) {
+                        float4* dst = chunk_ptr(j, c);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            __stcg(dst + v * kRowsPerCta,
+                                   make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+                    }
+                }
+                if (!owns_any)
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                __threadfence();
+                __syncwarp();
+                bool ready = true;
+                if (lane == 0) {
+                    atomicAdd(cnt, 1u);
+                    ready = wait_counter_at_least(cnt, uint32_t(S), p, abort_flag);
+                }
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                __threadfence();
+                if (owns_any) {
+                    int last_owned = c_begin;
+                    for (int c = c_begin; c < c_end; ++c)
+                        if (c % S == j)
+                            last_owned = c;
+#pragma unroll 1
+                    for (int c = c_begin; c < c_end; ++c) {
+                        if (c % S != j)
+                            continue;
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                        float4 acc[8];
+                        float4 x[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                        for (int i = 0; i < S; ++i) {
+                            if (i == j) {
+                                ptx::tmem_ld_wait();
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    x[v] = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            } else {
+                                const float4* src = chunk_ptr(i, c);
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    x[v] = (row_ok && ready) ? __ldcg(src + v * kRowsPerCta)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                            if (i == 0) {
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    acc[v] = x[v];
+                            } else {
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) {
+                                    acc[v].x += x[v].x;
+                                    acc[v].y += x[v].y;
+                                    acc[v].z += x[v].z;
+                                    acc[v].w += x[v].w;
+                                }
+                            }
+                        }
+                        ptx::tmem_ld_wait();
+                        if (c == last_owned)
+                            release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            r[4 * v + 0] = __float_as_uint(acc[v].x);
+                            r[4 * v + 1] = __float_as_uint(acc[v].y);
+                            r[4 * v + 2] = __float_as_uint(acc[v].z);
+                            r[4 * v + 3] = __float_as_uint(acc[v].w);
+                        }
+                        store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                    }
+                }
+                // second arrival: the slice that completes 2S has seen every other
+                // slice pass its wait, so it re-arms the counter for the next launch
+                __syncwarp();
+                if (lane == 0 && atomicAdd(cnt, 1u) == uint32_t(2 * S - 1))
+                    *cnt = 0u;
+                continue;
+            }
+
+            // ---- one piece of a tile's K range (split-K slice or stream-K piece).
+            // Pieces j = 0 .. P-1 in K order.  Pieces 1 .. P-1 store fp32 partials
+            // and count themselves in T; piece 0 -- under stream-K the last unit of
+            // its worker, so usually the last to finish -- waits until T = P - 1,
+            // then forms C = p_0 + ((p_1 + p_2) + ... + p_{P-1}) with p_0 straight
+            // from TMEM.  The order of the additions is fixed, so C is the same on
+            // every run; pieces 1.. never wait, so piece 0's wait always ends.
+            int pieces, j, first_worker = 0;
+            long long tile_it0 = 0;
+            int ctile;
+            if (w.kind == kUnitSplit) {
+                pieces = p.split_k;
+                j = w.split;
+                ctile = w.tile * CG + int(rank);
+            } else {
+                tile_it0 = (long long)w.sk_tile * p.num_k_blocks;
+                first_worker = sk_owner(p, tile_it0, workers);
+                pieces = sk_owner(p, tile_it0 + p.num_k_blocks - 1, workers) - first_worker + 1;
+                j = worker - first_worker;
+                ctile = w.sk_tile * CG + int(rank);
+            }
+            auto slot_of = [&](int i) -> size_t {  // CTA partial slot of piece i
+                if (w.kind == kUnitSplit)
+                    return size_t(w.tile * p.split_k + i) * CG + rank;
+                const int wi = first_worker + i;
+                const int si = (sk_begin(p, wi, workers) >= tile_it0) ? 0 : 1;
+                return size_t(wi * 2 + si) * CG + rank;
+            };
+            uint32_t* const cnt = p.tile_sems + size_t(ctile * kEpiWarps + ew) * kCountersPerWarp;
+            const bool row_ok = (cta_row0 + row) < p.M;  // padding rows move no bytes
+            // partial layout per CTA slot: [chunk][v = 0..7][row 0..127] float4
+            auto chunk_ptr = [&](size_t slot, int c) -> float4* {
+                return parts + slot * kSlotF4 + size_t(c) * 8 * kRowsPerCta + row;
+            };
+            auto load_chunk = [&](size_t slot, int c, float4 (&x)[8]) {
+                const float4* src = chunk_ptr(slot, c);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[v] = row_ok ? __ldcg(src + v * kRowsPerCta) : make_float4(0.f, 0.f, 0.f, 0.f);
+            };
+            auto add4 = [](float4& a, const float4& b) {
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            };
+
+            if (j == 0) {
+                bool ready = true;
+                if (lane == 0)
+                    ready = wait_counter(cnt, uint32_t(pieces - 1), p, abort_flag);
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (!ready) {
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                    continue;
+                }
+                __threadfence();
+#pragma unroll 1
+                for (int c = c_begin; c < c_end; ++c) {
+                    // S' = p_1 + ... + p_{P-1}, two pieces' loads in flight at a time
+                    float4 sp[8], x1[8];
+                    load_chunk(slot_of(1), c, sp);
+                    if (pieces > 2)
+                        load_chunk(slot_of(2), c, x1);
+                    if (pieces > 2) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            add4(sp[v], x1[v]);
+                    }
+#pragma unroll 1
+                    for (int i = 3; i < pieces; i += 2) {
+                        float4 y0[8], y1[8];
+                        load_chunk(slot_of(i), c, y0);
+                        if (i + 1 < pieces)
+                            load_chunk(slot_of(i + 1), c, y1);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            add4(sp[v], y0[v]);
+                        if (i + 1 < pieces) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                add4(sp[v], y1[v]);
+                        }
+                    }
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                    ptx::tmem_ld_wait();
+                    if (c == c_end - 1)
                         release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
-                    float4* pc = mine + size_t(c) * 8 * kRowsPerCta;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + sp[v].x);
+                        r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + sp[v].y);
+                        r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + sp[v].z);
+                        r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + sp[v].w);
+                    }
+                    store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    *cnt = 0u;  // every piece has arrived: re-armed for the next launch
+                continue;
+            }
+
+            // tail piece j >= 1: store this piece's partial, then count it
+            const size_t mine = slot_of(j);
+#pragma unroll 1
+            for (int c = c_begin; c < c_end; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                ptx::tmem_ld_wait();
+                if (c == c_end - 1)
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                if (row_ok) {
+                    float4* dst = chunk_ptr(mine, c);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        __stcg(pc + v * kRowsPerCta,
+                        __stcg(dst + v * kRowsPerCta,
                                make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
                                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
                 }
-                __threadfence();
-                __syncwarp();
-                uint32_t* counter = p.tile_sems + (ctile * kEpiWarps + q);
-                uint32_t last = 0;
-                if (lane == 0)
-                    last = (atomicAdd(counter, 1u) == uint32_t(S - 1)) ? 1u : 0u;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    __threadfence();
-#pragma unroll 1
-                    for (int c = 0; c < BN / kStoreCols; ++c) {
-                        float acc[32];
-                        const float4* pc = slot0 + size_t(c) * 8 * kRowsPerCta + row;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const float4 x = __ldcg(pc + v * kRowsPerCta);
-                            acc[4 * v + 0] = x.x;
-                            acc[4 * v + 1] = x.y;
-                            acc[4 * v + 2] = x.z;
-                            acc[4 * v + 3] = x.w;
-                        }
-#pragma unroll 1
-                        for (int j = 1; j < S; ++j) {
-                            const float4* pj = pc + size_t(j) * split_stride;
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                const float4 x = __ldcg(pj + v * kRowsPerCta);
-                                acc[4 * v + 0] += x.x;
-                                acc[4 * v + 1] += x.y;
-                                acc[4 * v + 2] += x.z;
-                                acc[4 * v + 3] += x.w;
-                            }
-                        }
-                        uint32_t r[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(acc[i]);
-                        store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols,
-                                  m_row);
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        *counter = 0u;  // re-armed for the next launch
-                }
             }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                atomicAdd(cnt, 1u);
         }
+        if (t > 0 && warp == 2 && lane == 0)
+            trace_unit(p, t - 1, 3);
         if (lane == 0)
             ptx::bulk_wait_group_all();
+        if (warp == 2 && lane == 0)
+            trace_mark(p, kTraceEpiDone);
         __syncwarp();
     }
 
@@ -455,6 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+        if (lane == 0)
+            trace_mark(p, kTraceExit);
     }
 }
 

@@ -8,7 +8,7 @@ namespace {
 
 template <int CG, int BN, int STAGES>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                       const GemmParams& p, int grid, cudaStream_t stream)
+                       const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
     auto kernel = gemm_kernel<CG, BN, STAGES>;
@@ -21,15 +21,22 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (CG == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, a, b, c, p);
 }
 
@@ -91,13 +98,13 @@ int variant_smem_bytes(int idx)
 }
 
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const GemmParams& p, int grid, cudaStream_t stream)
+                           const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     switch (idx) {
-    case 0: return launch_one<1, 256, 4>(a, b, c, p, grid, stream);
-    case 1: return launch_one<1, 128, 6>(a, b, c, p, grid, stream);
-    case 2: return launch_one<2, 256, 6>(a, b, c, p, grid, stream);
-    case 3: return launch_one<2, 128, 8>(a, b, c, p, grid, stream);
+    case 0: return launch_one<1, 256, 4>(a, b, c, p, grid, stream, pdl);
+    case 1: return launch_one<1, 128, 6>(a, b, c, p, grid, stream, pdl);
+    case 2: return launch_one<2, 256, 6>(a, b, c, p, grid, stream, pdl);
+    case 3: return launch_one<2, 128, 8>(a, b, c, p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

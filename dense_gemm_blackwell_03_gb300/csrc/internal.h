@@ -33,9 +33,11 @@ int find_variant(int cg, int bn);
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);
 
-// Launch variant `idx` with `grid` CTAs (a multiple of its CTA group).
+// Launch variant `idx` with `grid` CTAs (a multiple of its CTA group); with
+// `pdl`, as a programmatic dependent launch (its prologue may overlap the
+// previous kernel on the stream).
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const GemmParams& p, int grid, cudaStream_t stream);
+                           const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
 // Co-resident clusters (CTA pairs for cg == 2, CTAs for cg == 1) of variant
 // `idx` on the current device.
@@ -48,7 +50,12 @@ struct Selection {
     bwgemm_config_t cfg;
     int variant_idx;
     int num_m_blocks, num_n_blocks, num_k_blocks;
+    int64_t sk_iters;
 };
+
+// The launch description of a selection (pointers, timeout and the test hook
+// are left for the caller).
+GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype);
 
 // Host-only configuration choice (also behind bwgemm_select_config).
 bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, int64_t K,

@@ -17,8 +17,9 @@ enum : uint32_t {
 constexpr int kTileK = 64;             // K elements per pipeline stage (128 B rows: 128B swizzle)
 constexpr int kMmaK = 16;              // K per tcgen05.mma of kind::f16 (32 bytes)
 constexpr int kRowsPerCta = 128;       // accumulator rows per CTA (TMEM lanes)
-constexpr int kEpiWarps = 4;           // one warp per 32-lane quarter of TMEM
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, 4 epilogue warps
+constexpr int kEpiWarps = 8;           // two warps per 32-lane quarter of TMEM, half the columns each
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, 8 epilogue warps
+constexpr int kCountersPerWarp = 1;    // arrival counters per (tile, cta, epilogue warp)
 constexpr int kStoreCols = 32;         // columns per epilogue store box (64 B rows)
 
 #ifdef __CUDACC__
@@ -37,23 +38,49 @@ BWGEMM_HD constexpr uint32_t make_idesc(int dtype, int m, int n)
            (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
+// Work decomposition of one launch.  Tiles are numbered in grouped raster
+// order.  Tiles [0, dp_tiles) are "data-parallel": each is one unit, or
+// split_k slices of its K range (split-K).  Tiles [dp_tiles, num_tiles) form
+// the stream-K region: its sk_tiles * num_k_blocks K-block iterations are
+// divided evenly among the workers (CTA pairs, or CTAs for the 1-SM form);
+// a worker's range is cut at tile edges into pieces.  Every worker first
+// walks its stream-K range, then its data-parallel units (round robin).
 struct GemmParams {
     int32_t M, N, K;
     int32_t num_m_blocks;   // ceil(M / (CG * 128))
     int32_t num_n_blocks;   // ceil(N / BN)
     int32_t num_k_blocks;   // ceil(K / 64)
     int32_t num_tiles;      // num_m_blocks * num_n_blocks
-    int32_t split_k;        // >= 1; units = num_tiles * split_k
-    int32_t num_units;
+    int32_t split_k;        // >= 1 slices per data-parallel tile
+    int32_t dp_tiles;       // data-parallel tiles (ids [0, dp_tiles))
+    int32_t dp_units;       // dp_tiles * split_k
+    int32_t sk_tiles;       // stream-K tiles (ids [dp_tiles, num_tiles))
     int32_t raster_group;   // m-blocks per raster group (>= 1)
+    int64_t sk_iters;       // sk_tiles * num_k_blocks
     int32_t dtype;          // 0 = bf16, 1 = fp16 (inputs and output)
     uint32_t idesc;         // tcgen05 instruction descriptor
     uint64_t timeout_ns;    // bound on every device-side wait
     uint32_t* status;       // device status word
-    float* partials;        // split-K fp32 partial tiles (split_k > 1)
-    uint32_t* tile_sems;    // split-K per (tile, cta, warp) turn counters, zero between calls
-    int32_t stall_kblock;   // test hook: producer never fills this k-block of unit 0 (< 0: off)
+    float* partials;        // fp32 partial tiles of split-K slices / stream-K pieces
+    uint32_t* tile_sems;    // per (tile, cta, warp) arrival counters, zero between calls
+    int32_t stall_kblock;   // test hook: producer never fills this k-block of its first unit (< 0: off)
+    int32_t split_scatter;  // split-K in one wave: the slices of a tile reduce-scatter (see epilogue)
+    int32_t prefetch;       // K blocks the producer prefetches into L2 ahead of its loads (0: off)
     int32_t pad_;
+    uint64_t* trace;        // optional timeline: kTraceSlots %globaltimer stamps per CTA (null: off)
+};
+
+// Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).
+enum : int {
+    kTraceEntry = 0,          // kernel entry
+    kTraceReady = 1,          // barriers, TMEM and the dependency wait done
+    kTraceFirstLoad = 2,      // producer issues its first TMA load
+    kTraceLastLoad = 3,       // producer issued its last TMA load
+    kTraceEpiDone = 4,        // epilogue warp 2 finished (stores complete)
+    kTraceExit = 5,           // teardown done
+    kTraceUnit0 = 8,          // then per unit u < kTraceUnits: MMA start, MMA end,
+    kTraceUnits = 14,         //   epilogue start, epilogue end (4 slots each)
+    kTraceSlots = kTraceUnit0 + 4 * kTraceUnits,
 };
 
 }  // namespace bwgemm

@@ -153,7 +153,7 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     const int S = sel.cfg.split_k;
     const size_t tiles = size_t(sel.cfg.num_tiles);
     const size_t partial_bytes = tiles * size_t(S) * size_t(v.cg) * kRowsPerCta * size_t(v.bn) * 4;
-    const size_t counters = tiles * size_t(v.cg) * kEpiWarps;
+    const size_t counters = tiles * size_t(v.cg) * kEpiWarps * kCountersPerWarp;
     if (S > 1 && (partial_bytes > kNoAllocPartialBytes || counters > kNoAllocCounters))
         return BWGEMM_ERR_WORKSPACE;  // this shape's split-K scratch exceeds the fixed array
 
@@ -173,25 +173,12 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
         !encode(enc, &tc, C, dtype, N, M, ldc, kStoreCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return BWGEMM_ERR_CUDA;
 
-    GemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.M = int32_t(M);
-    p.N = int32_t(N);
-    p.K = int32_t(K);
-    p.num_m_blocks = sel.num_m_blocks;
-    p.num_n_blocks = sel.num_n_blocks;
-    p.num_k_blocks = sel.num_k_blocks;
-    p.num_tiles = sel.cfg.num_tiles;
-    p.split_k = S;
-    p.num_units = sel.cfg.num_units;
-    p.raster_group = sel.cfg.raster_group;
-    p.dtype = int32_t(dtype);
-    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
+    GemmParams p = make_params(sel, M, N, K, dtype);
     p.timeout_ns = 4000000000ull;
     p.status = status;
     p.tile_sems = ctr;
     p.partials = reinterpret_cast<float*>(partials);
-    p.stall_kblock = -1;
-    return launch_variant(sel.variant_idx, ta, tb, tc, p, sel.cfg.grid, s) == cudaSuccess ? BWGEMM_OK
-                                                                                          : BWGEMM_ERR_CUDA;
+    return launch_variant(sel.variant_idx, ta, tb, tc, p, sel.cfg.grid, s, false) == cudaSuccess
+               ? BWGEMM_OK
+               : BWGEMM_ERR_CUDA;
 }

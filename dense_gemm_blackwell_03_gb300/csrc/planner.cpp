@@ -48,7 +48,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     const int idx = find_variant(cg, bn);
     if (idx < 0)
         return BWGEMM_ERR_UNSUPPORTED;
-    if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0)
+    if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0 || opts.prefetch < -1 ||
+        opts.prefetch > 64)
         return BWGEMM_ERR_INVALID_ARG;
 
     const int tile_m = kRowsPerCta * cg;
@@ -59,34 +60,84 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     if (num_m > (1 << 30) || num_n > (1 << 30) || tiles > (int64_t(1) << 30))
         return BWGEMM_ERR_UNSUPPORTED;
 
-    // Concurrent work units the persistent grid holds.
+    // Workers (CTA pairs, or CTAs) the persistent grid holds at once.
     int64_t slots = (cg == 2) ? max_pairs : num_sms;
     if (opts.max_ctas > 0)
         slots = std::max<int64_t>(1, std::min<int64_t>(slots, opts.max_ctas / cg));
+    if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_STREAM_K)
+        return BWGEMM_ERR_INVALID_ARG;
 
-    // Split-K: when the tiles alone leave most of the GPU idle (decode-sized
-    // M), cut each tile's K range into s slices so that tiles * s fills the
-    // grid; keep at least 4 K blocks of 64 per slice.
-    int64_t s = 1;
-    if (opts.split_k > 0) {
-        s = std::min<int64_t>(opts.split_k, std::max<int64_t>(num_kb, 1));
-    } else if (tiles > 0 && tiles < slots && num_kb >= 8) {
-        s = std::min<int64_t>({slots / tiles, num_kb / 4, 8});
-        s = std::max<int64_t>(s, 1);
+    // Schedule.  Whole tiles when they fill the workers evenly.  With fewer
+    // tiles than workers: whole tiles when they still occupy >= 80 % of the
+    // workers; else split-K in one wave (S slices per tile, all running at
+    // once, reduce-scattering their partials) when S >= 2 fills >= 75 %;
+    // else stream-K.  With more tiles than workers but a ragged last wave
+    // (< 90 % full): stream-K -- the whole waves but the last one stay whole
+    // tiles and the K iterations of the remaining tiles are divided evenly.
+    bool stream_k = false;
+    int64_t auto_split = 1;
+    if (opts.split_k > 1 || opts.schedule == BWGEMM_SCHEDULE_TILES || tiles == 0) {
+        stream_k = false;
+    } else if (opts.schedule == BWGEMM_SCHEDULE_STREAM_K) {
+        stream_k = true;
+    } else if (num_kb >= 4 && tiles % slots != 0) {
+        if (tiles > slots) {
+            const int64_t waves = (tiles + slots - 1) / slots;
+            stream_k = double(tiles) / double(waves * slots) < 0.9;
+        } else if (double(tiles) < 0.8 * double(slots)) {
+            const int64_t S = std::min<int64_t>({slots / tiles, num_kb / 4, 4});
+            if (S >= 2 && double(tiles * S) >= 0.75 * double(slots))
+                auto_split = S;
+            else
+                stream_k = true;
+        }
     }
-    int64_t ws = 0;
-    if (s > 1) {
-        const int64_t counters = tiles * cg * kEpiWarps * 4;
-        ws = int64_t(kCounterRegionBytes) + tiles * s * cg * int64_t(kRowsPerCta) * bn * 4;
+
+    int64_t s = 1, dp_tiles = tiles, sk_tiles = 0, workers = 0, ws = 0;
+    const int64_t slot_bytes = int64_t(cg) * kRowsPerCta * bn * 4;  // one piece's fp32 partial
+    if (stream_k) {
+        dp_tiles = (tiles >= 2 * slots) ? (tiles / slots - 1) * slots : 0;
+        sk_tiles = tiles - dp_tiles;
+        const int64_t iters = sk_tiles * num_kb;
+        // at least 4 K blocks per worker; all workers when there are whole tiles too
+        workers = dp_tiles > 0 ? slots : std::max<int64_t>(1, std::min<int64_t>(slots, iters / 4));
+        ws = int64_t(kCounterRegionBytes) + workers * 2 * slot_bytes;
+        const int64_t counters = sk_tiles * cg * kEpiWarps * kCountersPerWarp * 4;
         if (counters > int64_t(kCounterRegionBytes) || uint64_t(ws) > workspace_bytes) {
-            if (opts.split_k > 1)
+            if (opts.schedule == BWGEMM_SCHEDULE_STREAM_K)
                 return BWGEMM_ERR_WORKSPACE;
-            s = 1;
+            stream_k = false;
+            dp_tiles = tiles;
+            sk_tiles = 0;
             ws = 0;
         }
     }
-    const int64_t units = tiles * s;
-    const int64_t clusters = std::min<int64_t>(units, slots);
+    if (!stream_k) {
+        // split-K over whole tiles: forced, chosen above, or (schedule = tiles)
+        // when the tiles alone leave most workers idle; >= 4 K blocks per slice
+        if (opts.split_k > 0) {
+            s = std::min<int64_t>(opts.split_k, std::max<int64_t>(num_kb, 1));
+        } else if (auto_split > 1) {
+            s = auto_split;
+        } else if (opts.schedule == BWGEMM_SCHEDULE_TILES && tiles > 0 && tiles < slots &&
+                   num_kb >= 8) {
+            s = std::min<int64_t>({slots / tiles, num_kb / 4, 8});
+            s = std::max<int64_t>(s, 1);
+        }
+        if (s > 1) {
+            const int64_t counters = tiles * cg * kEpiWarps * kCountersPerWarp * 4;
+            ws = int64_t(kCounterRegionBytes) + tiles * s * slot_bytes;
+            if (counters > int64_t(kCounterRegionBytes) || uint64_t(ws) > workspace_bytes) {
+                if (opts.split_k > 1)
+                    return BWGEMM_ERR_WORKSPACE;
+                s = 1;
+                ws = 0;
+            }
+        }
+        workers = std::min<int64_t>(tiles * s, slots);
+    }
+    // all slices of every tile in one wave: they may wait for one another
+    const bool scatter = !stream_k && s > 1 && tiles * s <= slots;
 
     int64_t group = opts.raster_group > 0 ? opts.raster_group : 8;
     group = std::max<int64_t>(1, std::min<int64_t>(group, std::max<int64_t>(num_m, 1)));
@@ -97,6 +148,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.num_m_blocks = int(num_m);
     sel.num_n_blocks = int(num_n);
     sel.num_k_blocks = int(num_kb);
+    sel.sk_iters = sk_tiles * num_kb;
     sel.cfg.variant = (cg == 2) ? BWGEMM_VARIANT_2SM : BWGEMM_VARIANT_1SM;
     sel.cfg.tile_m = tile_m;
     sel.cfg.tile_n = bn;
@@ -105,11 +157,42 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.cfg.split_k = int32_t(s);
     sel.cfg.raster_group = int32_t(group);
     sel.cfg.num_tiles = int32_t(tiles);
-    sel.cfg.num_units = int32_t(units);
-    sel.cfg.grid = int32_t(clusters * cg);
+    sel.cfg.num_units = int32_t(dp_tiles * s);
+    sel.cfg.grid = int32_t(workers * cg);
     sel.cfg.workspace_bytes = ws;
+    sel.cfg.schedule = stream_k ? BWGEMM_SCHEDULE_STREAM_K : BWGEMM_SCHEDULE_TILES;
+    sel.cfg.dp_tiles = int32_t(dp_tiles);
+    sel.cfg.sk_tiles = int32_t(sk_tiles);
+    sel.cfg.workers = int32_t(workers);
+    sel.cfg.split_scatter = scatter ? 1 : 0;
     *out = sel;
     return BWGEMM_OK;
+}
+
+GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype)
+{
+    const Variant& v = kVariants[sel.variant_idx];
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.M = int32_t(M);
+    p.N = int32_t(N);
+    p.K = int32_t(K);
+    p.num_m_blocks = sel.num_m_blocks;
+    p.num_n_blocks = sel.num_n_blocks;
+    p.num_k_blocks = sel.num_k_blocks;
+    p.num_tiles = sel.cfg.num_tiles;
+    p.split_k = sel.cfg.split_k;
+    p.dp_tiles = sel.cfg.dp_tiles;
+    p.dp_units = sel.cfg.num_units;
+    p.sk_tiles = sel.cfg.sk_tiles;
+    p.sk_iters = sel.sk_iters;
+    p.raster_group = sel.cfg.raster_group;
+    p.dtype = int32_t(dtype);
+    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
+    p.stall_kblock = -1;
+    p.split_scatter = sel.cfg.split_scatter;
+    p.prefetch = 0;  // L2 prefetch ahead of the loads measured slower on every shape
+    return p;
 }
 
 }  // namespace bwgemm

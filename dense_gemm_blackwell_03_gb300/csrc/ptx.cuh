@@ -43,6 +43,22 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Block until every grid this one depends on (the previous kernel on the
+// stream, when launched with programmatic stream serialisation) has completed
+// and its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream to be scheduled; it still runs its own
+// grid_dependency_wait before touching memory this grid writes.
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
@@ -158,6 +174,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// Prefetch one 2-D box of a tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // 2-D tiled store shared -> global (out-of-range rows/columns are clipped).

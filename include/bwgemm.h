@@ -38,7 +38,7 @@ extern "C" {
 #endif
 
 #define BWGEMM_VERSION_MAJOR 0
-#define BWGEMM_VERSION_MINOR 1
+#define BWGEMM_VERSION_MINOR 2
 
 typedef struct bwgemm_plan_s* bwgemm_plan_t;
 
@@ -64,6 +64,13 @@ typedef enum {
     BWGEMM_VARIANT_2SM = 2   /* CTA pair per tile: 256 x BN tiles, cta_group::2        */
 } bwgemm_variant_t;
 
+typedef enum {
+    BWGEMM_SCHEDULE_AUTO = 0,     /* stream-K when whole tiles leave workers idle         */
+    BWGEMM_SCHEDULE_TILES = 1,    /* whole tiles, or split_k slices of every tile          */
+    BWGEMM_SCHEDULE_STREAM_K = 2  /* K iterations of the last tiles divided evenly among
+                                     the workers; the earlier full waves as whole tiles    */
+} bwgemm_schedule_t;
+
 /* Plan options.  Zero means "choose automatically" for every field; get the
  * defaults with bwgemm_default_options(). */
 typedef struct {
@@ -76,8 +83,14 @@ typedef struct {
                                  this k-block of its first unit, so a bounded wait runs
                                  out and the call reports BWGEMM_ERR_TIMEOUT            */
     uint64_t timeout_ns;      /* bound on every device-side wait; 0 = 4 s               */
-    uint64_t workspace_bytes; /* split-K workspace owned by the plan; 0 = 64 MiB        */
-    int32_t reserved[8];      /* must be zero                                            */
+    uint64_t workspace_bytes; /* split-K / stream-K workspace of the plan; 0 = 64 MiB   */
+    int32_t schedule;         /* bwgemm_schedule_t                                       */
+    int32_t pdl_off;          /* nonzero: launch without programmatic dependent launch  */
+    int32_t trace;            /* nonzero: record a per-CTA timeline of every launch
+                                 (read back with bwgemm_plan_read_trace)                */
+    int32_t prefetch;         /* K blocks of A and B prefetched into L2 ahead of the
+                                 shared-memory loads: 0 = default (none), -1 = none     */
+    int32_t reserved[4];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -90,9 +103,16 @@ typedef struct {
     int32_t split_k;      /* K slices per tile (1 = none)                        */
     int32_t raster_group; /* m-blocks per raster group                           */
     int32_t num_tiles;    /* output tiles                                        */
-    int32_t num_units;    /* tiles x split_k                                     */
+    int32_t num_units;    /* whole-tile / split-K units (dp_tiles x split_k)     */
     int32_t grid;         /* CTAs launched (persistent)                          */
-    int64_t workspace_bytes; /* split-K bytes used by this shape                 */
+    int64_t workspace_bytes; /* partial-tile bytes used by this shape            */
+    int32_t schedule;     /* BWGEMM_SCHEDULE_TILES or BWGEMM_SCHEDULE_STREAM_K   */
+    int32_t dp_tiles;     /* tiles computed whole (or as split_k slices)         */
+    int32_t sk_tiles;     /* tiles whose K iterations are spread by stream-K     */
+    int32_t workers;      /* CTAs or CTA pairs of the persistent grid            */
+    int32_t split_scatter; /* 1: the split_k slices of each tile run in one wave
+                              and reduce-scatter their partials                  */
+    int32_t reserved;
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */
@@ -172,6 +192,20 @@ bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t
 
 /* The configuration of the plan's most recent bwgemm_run / bwgemm_run_host. */
 bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out);
+
+/*
+ * Timeline of the plan's most recent launch (plans created with opts.trace):
+ * synchronises the device, then copies ctas x slots %globaltimer stamps
+ * (nanoseconds; 0 = not reached) into `out`, row per CTA.  Slots: 0 kernel
+ * entry, 1 prologue and dependency wait done, 2 first TMA load issued,
+ * 3 last TMA load issued, 4 epilogue finished, 5 exit; from slot 8 on, four
+ * per work unit (at most 14 units): MMA start, MMA end, epilogue start,
+ * epilogue end.  *ctas and *slots receive the dimensions; `capacity` is the
+ * size of `out` in elements.  BWGEMM_ERR_INVALID_ARG if tracing is off or
+ * `out` is too small.
+ */
+bwgemm_status_t bwgemm_plan_read_trace(bwgemm_plan_t plan, uint64_t* out, int64_t capacity,
+                                       int32_t* ctas, int32_t* slots);
 
 /* Number of GEMM kernels the plan has enqueued since it was created. */
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);

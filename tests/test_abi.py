@@ -46,9 +46,10 @@ def test_struct_layout_matches_header(tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "bwgemm.h"\n'
         "int main(void) {\n"
-        '  printf("%zu %zu %zu %zu\\n", sizeof(bwgemm_plan_options_t), '
-        "offsetof(bwgemm_plan_options_t, timeout_ns), sizeof(bwgemm_config_t), "
-        "offsetof(bwgemm_config_t, workspace_bytes));\n"
+        '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(bwgemm_plan_options_t), '
+        "offsetof(bwgemm_plan_options_t, timeout_ns), offsetof(bwgemm_plan_options_t, pdl_off), "
+        "sizeof(bwgemm_config_t), offsetof(bwgemm_config_t, workspace_bytes), "
+        "offsetof(bwgemm_config_t, split_scatter));\n"
         "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -56,11 +57,12 @@ def test_struct_layout_matches_header(tmp_path):
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
                                           text=True).stdout.split()]
     assert got == [ctypes.sizeof(PlanOptions), PlanOptions.timeout_ns.offset,
-                   ctypes.sizeof(Config), Config.workspace_bytes.offset]
+                   PlanOptions.pdl_off.offset, ctypes.sizeof(Config), Config.workspace_bytes.offset,
+                   Config.split_scatter.offset]
 
 
 def test_version_and_status_strings(lib):
-    assert lib.bwgemm_version() == (0 << 16) | 1
+    assert lib.bwgemm_version() == (0 << 16) | 2
     for code in range(8):
         assert lib.bwgemm_status_string(code)
     assert lib.bwgemm_status_string(99) == b"unknown status"
@@ -104,32 +106,79 @@ def cfg(M, N, K, sms=148, pairs=0, **opts):
     return binding.select_config(sms, M, N, K, max_pairs=pairs, **opts)
 
 
-def test_select_square_uses_cta_pairs():
+def test_select_square_uses_cta_pairs_and_stream_k():
+    # 4096^3: 256 tiles of 256 x 256 over 76 pairs = 3.37 waves.  Two whole
+    # waves stay whole tiles; the K iterations of the other 104 tiles are
+    # divided evenly among the 76 pairs.
     c = cfg(4096, 4096, 4096, sms=152, pairs=76)
     assert c["variant"] == 2 and c["tile_m"] == 256 and c["tile_n"] == 256
-    assert c["num_tiles"] == 16 * 16 and c["split_k"] == 1
-    assert c["grid"] == 2 * 76 and c["tile_k"] == 64 and c["stages"] == 6
+    assert c["num_tiles"] == 16 * 16 and c["split_k"] == 1 and c["stages"] == 6
+    assert c["schedule"] == binding.SCHEDULE_STREAM_K
+    assert c["dp_tiles"] == 152 and c["sk_tiles"] == 104 and c["workers"] == 76
+    assert c["grid"] == 152 and c["num_units"] == 152
+    assert c["workspace_bytes"] == (1 << 20) + 76 * 2 * 2 * 128 * 256 * 4
 
 
-def test_select_small_m_uses_single_cta_tiles():
+def test_select_even_waves_stay_whole_tiles():
+    # 8192 x 8192: 1024 tiles over 76 pairs = 13.5 waves (96 % full): whole tiles
+    c = cfg(8192, 8192, 8192, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["dp_tiles"] == 1024
+    assert c["sk_tiles"] == 0 and c["workspace_bytes"] == 0 and c["grid"] == 152
+    # tiles that fill the workers exactly
+    c = cfg(4096, 4096, 4096, sms=152, pairs=64)
+    assert c["schedule"] == binding.SCHEDULE_TILES
+
+
+def test_select_small_m_splits_k_in_one_wave():
     c = cfg(64, 8192, 8192, sms=152, pairs=76)
-    assert c["variant"] == 1 and c["tile_m"] == 128
-    assert c["num_tiles"] == 32
-    # few tiles: K is split so that tiles x splits fills the GPU
-    assert c["split_k"] == 4 and c["num_units"] == 128 and c["grid"] == 128
+    assert c["variant"] == 1 and c["tile_m"] == 128 and c["num_tiles"] == 32
+    # fewer tiles than SMs: 4 K slices per tile, all 128 slices in one wave,
+    # reduce-scattering their partials
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 4
+    assert c["split_scatter"] == 1 and c["grid"] == 128
 
 
-def test_select_decode_splits_k():
-    c = cfg(256, 8192, 8192, sms=152, pairs=76)
-    assert c["variant"] == 2 and c["num_tiles"] == 32 and c["split_k"] == 2
-    assert c["num_units"] == 64 and c["grid"] == 128
+def test_select_decode_shapes():
+    # attention out / MLP down: 32 tiles of 256 x 256 over 76 pairs -> 2 slices each
+    for N, K in ((8192, 8192), (8192, 28672)):
+        c = cfg(256, N, K, sms=152, pairs=76)
+        assert c["variant"] == 2 and c["num_tiles"] == 32 and c["split_k"] == 2
+        assert c["split_scatter"] == 1 and c["grid"] == 128
+    # fused QKV: 40 tiles, 2 slices would not fit one wave -> stream-K over all pairs
+    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
+    # MLP up: 112 tiles = 1.47 waves -> stream-K
+    c = cfg(256, 28672, 8192, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["dp_tiles"] == 0
+    # Gemma-like 512 x 8192 x 5376: 64 tiles fill 84 % of the pairs -> whole tiles
+    c = cfg(512, 8192, 5376, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 128
+
+
+def test_select_tiles_schedule_splits_k():
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES)
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2
+    assert c["num_units"] == 64 and c["grid"] == 128 and c["split_scatter"] == 1
     assert c["workspace_bytes"] == (1 << 20) + 32 * 2 * 2 * 128 * 256 * 4
+    # more slices than one wave holds: no reduce-scatter (slices may not wait)
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, split_k=3)
+    assert c["split_k"] == 3 and c["split_scatter"] == 0
+
+
+def test_select_small_problems_use_few_workers():
+    # 512^3: 4 tiles x 8 K blocks = 32 iterations, at least 4 per worker
+    c = cfg(512, 512, 512, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 8 and c["grid"] == 16
+    # fewer than 4 K blocks: nothing to spread
+    c = cfg(512, 512, 128, sms=152, pairs=76)
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["grid"] == 8
 
 
 def test_select_forced_options():
     c = cfg(1024, 1024, 4096, variant=1, tile_n=128, split_k=3, raster_group=4, max_ctas=64)
     assert (c["variant"], c["tile_m"], c["tile_n"], c["stages"]) == (1, 128, 128, 6)
     assert c["split_k"] == 3 and c["raster_group"] == 4 and c["grid"] == 64
+    assert c["schedule"] == binding.SCHEDULE_TILES
     assert c["num_tiles"] == 64 and c["num_units"] == 192
     # a forced split whose partials do not fit the workspace is refused
     with pytest.raises(binding.BwgemmError) as e:
@@ -147,6 +196,13 @@ def test_select_rejects_bad_options():
     with pytest.raises(binding.BwgemmError) as e:
         cfg(256, 8192, 8192, split_k=4, workspace_bytes=1 << 20)
     assert e.value.status == WORKSPACE
+    with pytest.raises(binding.BwgemmError) as e:
+        cfg(4096, 4096, 4096, schedule=binding.SCHEDULE_STREAM_K, workspace_bytes=1 << 20)
+    assert e.value.status == WORKSPACE
+    with pytest.raises(binding.BwgemmError):
+        cfg(512, 512, 512, schedule=3)
+    # automatic stream-K falls back to whole tiles when the workspace is too small
+    assert cfg(4096, 4096, 4096, workspace_bytes=1 << 20)["schedule"] == binding.SCHEDULE_TILES
 
 
 def test_select_degenerate_shapes():

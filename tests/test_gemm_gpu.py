@@ -112,11 +112,90 @@ def test_split_k_exact_and_deterministic(variant, split):
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("split,max_ctas", [(2, 0), (3, 0), (4, 0), (3, 4), (4, 6)])
+def test_split_k_reduce_scatter_and_multi_wave(variant, split, max_ctas):
+    # max_ctas = 0: every slice of every tile in one wave (reduce-scatter);
+    # a small grid forces several waves, where slices may not wait on each other
+    A = make_matrix(300, 2048, "int2", seed=950 + split, device="cuda")
+    B = make_matrix(520, 2048, "int2", seed=960 + split, device="cuda")
+    with binding.Plan(0, variant=variant, split_k=split, max_ctas=max_ctas) as p:
+        _, C1 = run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["split_k"] == split
+        assert c["split_scatter"] == (1 if max_ctas == 0 else 0)
+        C2 = p.gemm(A, B)
+        assert p.status() == 0
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
 def test_split_k_normal_inputs():
     A = make_matrix(200, 4096, "normal", seed=910, device="cuda")
     B = make_matrix(384, 4096, "weight", seed=911, device="cuda")
     with binding.Plan(0, split_k=4) as p:
         run_full(p, A, B, "bf16")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("M,N,K,max_ctas", [
+    (512, 512, 512, 0),       # fewer tiles than workers: every tile split across workers
+    (1024, 1024, 1280, 6),    # 16 tiles on 3 pairs / 6 CTAs: whole waves + stream-K tail
+    (768, 1280, 4096, 8),     # pieces spanning several tiles per worker
+    (5, 768, 2000, 0),        # mostly padding rows: predicated partial traffic
+    (130, 264, 1600, 0),      # ragged M, N and K
+])
+def test_stream_k_exact(variant, M, N, K, max_ctas):
+    A = make_matrix(M, K, "int2", seed=1000 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=1100 + N, device="cuda")
+    with binding.Plan(0, variant=variant, schedule=binding.SCHEDULE_STREAM_K,
+                      max_ctas=max_ctas) as p:
+        _, C1 = run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["sk_tiles"] > 0
+        C2 = p.gemm(A, B)
+        assert p.status() == 0
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))  # deterministic
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_stream_k_normal_inputs(dtype):
+    A = make_matrix(1000, 3000, "normal", dtype, seed=1200, device="cuda")
+    B = make_matrix(696, 3000, "weight", dtype, seed=1201, device="cuda")
+    with binding.Plan(0, schedule=binding.SCHEDULE_STREAM_K, max_ctas=10) as p:
+        run_full(p, A, B, dtype)
+        assert p.last_config()["dp_tiles"] > 0
+
+
+def test_schedules_agree_on_integers():
+    A = make_matrix(640, 1536, "int2", seed=1300, device="cuda")
+    B = make_matrix(896, 1536, "int2", seed=1301, device="cuda")
+    outs = []
+    for sched in (binding.SCHEDULE_TILES, binding.SCHEDULE_STREAM_K, binding.SCHEDULE_AUTO):
+        with binding.Plan(0, schedule=sched) as p:
+            outs.append(p.gemm(A, B))
+            assert p.status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_without_programmatic_dependent_launch():
+    A = make_matrix(512, 512, "int2", seed=1400, device="cuda")
+    B = make_matrix(512, 512, "int2", seed=1401, device="cuda")
+    with binding.Plan(0, pdl_off=1) as p:
+        run_full(p, A, B, "bf16", exact=True)
+
+
+def test_back_to_back_launches_see_previous_results(plan):
+    # with programmatic dependent launch the next GEMM's prologue overlaps the
+    # previous one; the chain C1 = A B^T, C2 = C1 B^T must still read finished data
+    A = make_matrix(384, 256, "int2", seed=1500, device="cuda")
+    B = make_matrix(256, 256, "int2", seed=1501, device="cuda")
+    C1 = plan.gemm(A, B)            # 384 x 256, exact small integers
+    C2 = plan.gemm(C1, B)           # reads C1 right after it is written
+    assert plan.status() == 0
+    ref1 = oracle.gemm(bits_of(A), bits_of(B), "bf16")
+    compare(bits_of(C1), ref1, "bf16", 256, exact=True)
+    ref2 = oracle.gemm(ref1, bits_of(B), "bf16")
+    compare(bits_of(C2), ref2, "bf16", 256)
 
 
 def test_persistent_grid_smaller_than_units():
@@ -194,3 +273,26 @@ def test_full_square_integers_bit_exact(plan):
     ref = oracle.gemm(bits_of(A), bits_of(B), "bf16", rows=rows)
     compare(bits_of(C[torch.from_numpy(rows).cuda()]), ref, "bf16", 4096, exact=True)
     del s
+
+
+def test_timeline_trace_is_ordered():
+    from dense_gemm_blackwell_03_gb300 import timeline
+    A = make_matrix(1024, 2048, "int2", seed=1600, device="cuda")
+    B = make_matrix(1536, 2048, "int2", seed=1601, device="cuda")
+    with binding.Plan(0, trace=1, max_ctas=16) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        tr = p.read_trace().astype(np.int64)
+        c = p.last_config()
+    assert tr.shape == (c["grid"], 64)
+    for row in tr:
+        e, r, f, l, d, x = (row[i] for i in range(6))
+        assert 0 < e <= r <= f <= l <= x and r <= d <= x
+    s = timeline.summarize(tr)
+    assert s["ctas"] == c["grid"] and s["span_us"] > 0
+    assert s["units_per_cta"]["max"] >= 2
+    for ulist in timeline.units(tr):
+        for ms, me, es, ee in ulist:
+            if ms and me:
+                assert ms <= me
+            if es and ee:
+                assert es <= ee

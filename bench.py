@@ -195,6 +195,20 @@ def time_each(fn, sets, iters, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def aggregate(local_seconds: float, work_per_step: float, steps: int, dist=None, device="cpu"):
+    """Whole-job throughput of N replicas: the max time over ranks, all ranks'
+    work.  Returns (max_seconds, work_per_second)."""
+    world = 1
+    t = local_seconds
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        buf = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+        dist.all_reduce(buf, op=dist.ReduceOp.MAX)
+        t = float(buf.item())
+    return t, world * work_per_step * steps / t
+
+
 def roofline_entry(shape, seconds, peaks):
     """Bound, achieved and peak for one shape (the min(peak, AI x BW) roofline)."""
     flops = shape.flops
@@ -334,13 +348,9 @@ def run_ours(args):
     kcfg = plan.last_config()
     per = time_each(ours, sets, max(50, min(args.steps, 200)), stream)
 
-    total_s = total_ms / 1e3
-    if dist:
-        t = torch.tensor([total_s], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s, flops_per_s = aggregate(total_ms / 1e3, shape.flops, args.steps, dist, device)
     ms_per_step = total_s * 1e3 / args.steps
-    value = world * shape.flops * args.steps / total_s / 1e12
+    value = flops_per_s / 1e12
     per_sorted = sorted(per)
     median_ms = statistics.median(per)
     avg_launch_s = total_s / args.steps  # one kernel launch per step, back to back
@@ -348,6 +358,8 @@ def run_ours(args):
     roof = roofline_entry(shape, avg_launch_s, peaks)
     roofline = {"bound": roof["bound"], "achieved": roof["achieved"], "peak": roof["peak"],
                 "unit": roof["unit"], "frac": roof["frac"],
+                "frac_of_sustained_peak": (round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
+                                           if roof["bound"] == "tensor" else None),
                 "traffic": recorded_traffic(shape.name),
                 "peak_source": f"{peaks['source']} ({'burst cuBLAS bf16' if roof['bound'] == 'tensor' else 'copy bandwidth'})",
                 "kernel": "bwgemm::gemm_kernel (persistent tcgen05)",
@@ -358,8 +370,8 @@ def run_ours(args):
     # cuBLAS (torch.matmul) on the same tensors, as same-box context
     def cublas(A, B, C):
         torch.matmul(A, B.t(), out=C)
-    cb_ms = time_region(cublas, sets, min(args.steps, 300), 5, stream, barrier)
-    cb_s = cb_ms / 1e3 / min(args.steps, 300)
+    cb_ms = time_region(cublas, sets, args.steps, 5, stream, barrier)
+    cb_s = cb_ms / 1e3 / args.steps
 
     # end-to-end through the C ABI with host buffers (H2D of A, B and D2H of C each step)
     e2e = None
@@ -376,12 +388,8 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             plan.gemm_host(hA, hB, out=hC, stream=stream)
-        e2e_s = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([e2e_s], device=device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": round(world * shape.flops * e2e_steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+        e2e_s, e2e_flops = aggregate(time.perf_counter() - t0, shape.flops, e2e_steps, dist, device)
+        e2e = {"value": round(e2e_flops / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": 2 * (shape.M * shape.K + shape.N * shape.K),
                "d2h_bytes_per_step": 2 * shape.M * shape.N, "steps": e2e_steps,
                "api": "bwgemm_run_host (pinned host A, B, C)"}
@@ -462,7 +470,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--shape", default=HEADLINE)

@@ -65,7 +65,8 @@ class PlanOptions(ctypes.Structure):
         ("pdl_off", ctypes.c_int32),
         ("trace", ctypes.c_int32),
         ("prefetch", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("swap_ab", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -87,7 +88,7 @@ class Config(ctypes.Structure):
         ("sk_tiles", ctypes.c_int32),
         ("workers", ctypes.c_int32),
         ("split_scatter", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("swap_ab", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

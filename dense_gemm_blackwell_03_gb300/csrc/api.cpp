@@ -141,16 +141,21 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
         return BWGEMM_OK;
     }
     Selection sel;
-    st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256)], M, N, K, plan->opts,
+    st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256, false)], M, N, K, plan->opts,
                        plan->workspace_bytes, &sel);
     if (st != BWGEMM_OK)
         return st;
     const Variant& v = kVariants[sel.variant_idx];
     const uint32_t b_rows = uint32_t(v.cg == 1 ? v.bn : v.bn / 2);
-    if ((st = get_tmap(plan->tmaps[0], A, dtype, K, M, lda, kTileK, kRowsPerCta,
+    // the MMA's A operand (128-row side) and B operand; exchanged when swapped
+    const void* opA = sel.swap ? B : A;
+    const void* opB = sel.swap ? A : B;
+    const int64_t rowsA = sel.swap ? N : M, rowsB = sel.swap ? M : N;
+    const int64_t ldA = sel.swap ? ldb : lda, ldB = sel.swap ? lda : ldb;
+    if ((st = get_tmap(plan->tmaps[0], opA, dtype, K, rowsA, ldA, kTileK, kRowsPerCta,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK)
         return st;
-    if ((st = get_tmap(plan->tmaps[1], B, dtype, K, N, ldb, kTileK, b_rows,
+    if ((st = get_tmap(plan->tmaps[1], opB, dtype, K, rowsB, ldB, kTileK, b_rows,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK)
         return st;
     if ((st = get_tmap(plan->tmaps[2], C, dtype, N, M, ldc, kStoreCols, 32,
@@ -356,18 +361,23 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
         (st = grow(plan->h2d[1], plan->h2d_cap[1], size_t(N) * dlda * 2)) != BWGEMM_OK ||
         (st = grow(plan->h2d[2], plan->h2d_cap[2], size_t(M) * dldc * 2)) != BWGEMM_OK)
         return st;
+    // one linear copy when the host rows are already packed like the device copy
+    auto copy_rows = [&](void* dst, int64_t dld, const void* src, int64_t sld, int64_t cols,
+                         int64_t rows, cudaMemcpyKind kind) {
+        if (sld == dld && dld == cols)
+            return cudaMemcpyAsync(dst, src, size_t(rows) * size_t(cols) * 2, kind, s);
+        return cudaMemcpy2DAsync(dst, size_t(dld) * 2, src, size_t(sld) * 2, size_t(cols) * 2,
+                                 size_t(rows), kind, s);
+    };
     if (K > 0) {
-        if (cudaMemcpy2DAsync(plan->h2d[0], size_t(dlda) * 2, A_host, size_t(lda) * 2, size_t(K) * 2,
-                              size_t(M), cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpy2DAsync(plan->h2d[1], size_t(dlda) * 2, B_host, size_t(ldb) * 2, size_t(K) * 2,
-                              size_t(N), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        if (copy_rows(plan->h2d[0], dlda, A_host, lda, K, M, cudaMemcpyHostToDevice) != cudaSuccess ||
+            copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice) != cudaSuccess)
             return BWGEMM_ERR_CUDA;
     }
     st = enqueue(plan, plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N, K, dlda, dlda, dldc, dtype, s);
     if (st != BWGEMM_OK)
         return st;
-    if (cudaMemcpy2DAsync(C_host, size_t(ldc) * 2, plan->h2d[2], size_t(dldc) * 2, size_t(N) * 2,
-                          size_t(M), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (copy_rows(C_host, ldc, plan->h2d[2], dldc, N, M, cudaMemcpyDeviceToHost) != cudaSuccess)
         return BWGEMM_ERR_CUDA;
     return bwgemm_get_status(plan, stream);
 }

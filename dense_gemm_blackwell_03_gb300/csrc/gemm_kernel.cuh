@@ -33,6 +33,10 @@
 //   Kernel 5.
 //   TMEM accumulator ring (accum_full / accum_empty), persistent CTAs:
 //   deep dive Kernel 8.  Grouped rasterisation for L2 reuse: Kernel 9.
+//
+// TR = true runs the same pipeline on swapped operands (C^T = B A^T: the
+// N x K operand fills the 128-row MMA side, the few rows of a small-M
+// problem become the MMA's N) and writes each accumulator box transposed.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -279,41 +283,69 @@ __device__ __forceinline__ void release_accumulator(uint32_t bar, int lane)
     }
 }
 
-// Convert one thread's 32 fp32 values (one row, 32 consecutive columns) and
-// stage the warp's 32 x 32 box in shared memory with the 64-byte swizzle the
-// C tensor map uses (16-byte chunk index XOR bits 7-8 of the offset), then
-// TMA-store it.  Two staging buffers per warp alternate; a buffer is reused
-// only after the bulk store issued from it two boxes earlier finished reading.
+// Convert one thread's 32 fp32 values (one accumulator row, 32 consecutive
+// columns) and stage the warp's 32 x 32 box in shared memory with the 64-byte
+// swizzle the C tensor map uses (16-byte chunk index XOR bits 7-8 of the
+// offset), then TMA-store it.  `m_row` is the accumulator row of lane 0,
+// `col` the accumulator column of value 0.  With TR (swapped operands, the
+// accumulator holds C transposed) the box is written transposed: accumulator
+// rows are C columns and accumulator columns are C rows.  Two staging buffers
+// per warp alternate; a buffer is reused only after the bulk store issued
+// from it two boxes earlier finished reading.
+template <bool TR>
 __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmParams& p,
                                           const CUtensorMap* tmap_c, uint32_t my_store,
                                           int& chunk_ctr, int lane, int col, int m_row)
 {
     constexpr int kBufBytes = 32 * kStoreCols * 2;
-    uint32_t packed[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
     const uint32_t sb = my_store + uint32_t((chunk_ctr & 1) * kBufBytes);
-    if (lane == 0)
-        ptx::bulk_wait_group_read<1>();
-    __syncwarp();
-    const uint32_t row_addr = sb + uint32_t(lane * 64);
-    const uint32_t swz = uint32_t((lane >> 1) & 3);
+    if constexpr (!TR) {
+        uint32_t packed[16];
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-        ptx::st_shared_v4(row_addr + ((uint32_t(ch) ^ swz) << 4), packed[4 * ch + 0],
-                          packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+        for (int i = 0; i < 16; ++i)
+            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
+        if (lane == 0)
+            ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t row_addr = sb + uint32_t(lane * 64);
+        const uint32_t swz = uint32_t((lane >> 1) & 3);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            ptx::st_shared_v4(row_addr + ((uint32_t(ch) ^ swz) << 4), packed[4 * ch + 0],
+                              packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+    } else {
+        // box row i = C row (col + i), box column lane = C column (m_row + lane)
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
+        if (lane == 0)
+            ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t in_chunk = uint32_t((lane & 7) * 2);
+        const uint32_t chunk = uint32_t(lane >> 3);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t addr = sb + uint32_t(i * 64) + ((chunk ^ uint32_t((i >> 1) & 3)) << 4) + in_chunk;
+            const uint32_t h = (i & 1) ? (packed[i >> 1] >> 16) : (packed[i >> 1] & 0xFFFFu);
+            ptx::st_shared_u16(addr, uint16_t(h));
+        }
+    }
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (m_row < p.M && col < p.N)  // boxes wholly outside C are skipped
-            ptx::tma_store_2d(tmap_c, sb, col, m_row);
+        if (m_row < p.M && col < p.N) {  // boxes wholly outside C are skipped
+            if constexpr (!TR)
+                ptx::tma_store_2d(tmap_c, sb, col, m_row);
+            else
+                ptx::tma_store_2d(tmap_c, sb, m_row, col);
+        }
         ptx::bulk_commit_group();
     }
     ++chunk_ctr;
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool TR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
@@ -543,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait();
                     if (c == c_end - 1)
                         release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
-                    store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
                 }
                 continue;
             }
@@ -564,11 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t slot = size_t(w.tile * S + slice) * CG + rank;
                     return parts + slot * kSlotF4 + size_t(c) * 8 * kRowsPerCta + row;
                 };
+                // store the chunks other slices own
                 bool owns_any = false;
+                int last_owned = c_begin;
 #pragma unroll 1
                 for (int c = c_begin; c < c_end; ++c) {
                     if (c % S == j) {
                         owns_any = true;
+                        last_owned = c;
                         continue;
                     }
                     uint32_t r[32];
@@ -585,20 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!owns_any)
                     release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
-                __threadfence();
+                // publish: the warp barrier orders every lane's stores before lane
+                // 0's release-add; the slice that arrives last need not poll
                 __syncwarp();
                 bool ready = true;
                 if (lane == 0) {
-                    atomicAdd(cnt, 1u);
-                    ready = wait_counter_at_least(cnt, uint32_t(S), p, abort_flag);
+                    const uint32_t old = ptx::atom_add_release_gpu(cnt, 1u);
+                    if (old + 1u < uint32_t(S))
+                        ready = wait_counter_at_least(cnt, uint32_t(S), p, abort_flag);
                 }
                 ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                 __threadfence();
                 if (owns_any) {
-                    int last_owned = c_begin;
-                    for (int c = c_begin; c < c_end; ++c)
-                        if (c % S == j)
-                            last_owned = c;
 #pragma unroll 1
                     for (int c = c_begin; c < c_end; ++c) {
                         if (c % S != j)
@@ -649,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             r[4 * v + 2] = __float_as_uint(acc[v].z);
                             r[4 * v + 3] = __float_as_uint(acc[v].w);
                         }
-                        store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                        store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
                     }
                 }
                 // second arrival: the slice that completes 2S has seen every other
@@ -756,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + sp[v].z);
                         r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + sp[v].w);
                     }
-                    store_box(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
                 }
                 __syncwarp();
                 if (lane == 0)

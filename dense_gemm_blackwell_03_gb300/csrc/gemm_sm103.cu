@@ -6,12 +6,12 @@ namespace bwgemm {
 
 namespace {
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool TR>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -40,11 +40,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     return cudaLaunchKernelEx(&cfg, kernel, a, b, c, p);
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, bool TR>
 cudaError_t max_active_one(int* out)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -76,48 +76,51 @@ cudaError_t max_active_one(int* out)
     return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
 }
 
+struct VariantFns {
+    cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                          const GemmParams&, int, cudaStream_t, bool);
+    cudaError_t (*max_active)(int*);
+    int smem_bytes;
+};
+
+#define BWGEMM_VARIANT(CG, BN, ST, TR) \
+    {&launch_one<CG, BN, ST, TR>, &max_active_one<CG, BN, ST, TR>, KernelConfig<CG, BN, ST>::kSmemBytes}
+
+// same order as kVariants in internal.h
+constexpr VariantFns kFns[] = {
+    BWGEMM_VARIANT(1, 256, 4, false), BWGEMM_VARIANT(1, 128, 6, false),
+    BWGEMM_VARIANT(2, 256, 6, false), BWGEMM_VARIANT(2, 128, 8, false),
+    BWGEMM_VARIANT(2, 128, 8, true),  BWGEMM_VARIANT(2, 64, 9, true),
+    BWGEMM_VARIANT(1, 128, 6, true),  BWGEMM_VARIANT(1, 64, 8, true),
+};
+#undef BWGEMM_VARIANT
+static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");
+
 }  // namespace
 
-int find_variant(int cg, int bn)
+int find_variant(int cg, int bn, bool trans)
 {
     for (int i = 0; i < kNumVariants; ++i)
-        if (kVariants[i].cg == cg && kVariants[i].bn == bn)
+        if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans)
             return i;
     return -1;
 }
 
-int variant_smem_bytes(int idx)
-{
-    switch (idx) {
-    case 0: return KernelConfig<1, 256, 4>::kSmemBytes;
-    case 1: return KernelConfig<1, 128, 6>::kSmemBytes;
-    case 2: return KernelConfig<2, 256, 6>::kSmemBytes;
-    case 3: return KernelConfig<2, 128, 8>::kSmemBytes;
-    default: return 0;
-    }
-}
+int variant_smem_bytes(int idx) { return (idx >= 0 && idx < kNumVariants) ? kFns[idx].smem_bytes : 0; }
 
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
-    switch (idx) {
-    case 0: return launch_one<1, 256, 4>(a, b, c, p, grid, stream, pdl);
-    case 1: return launch_one<1, 128, 6>(a, b, c, p, grid, stream, pdl);
-    case 2: return launch_one<2, 256, 6>(a, b, c, p, grid, stream, pdl);
-    case 3: return launch_one<2, 128, 8>(a, b, c, p, grid, stream, pdl);
-    default: return cudaErrorInvalidValue;
-    }
+    if (idx < 0 || idx >= kNumVariants)
+        return cudaErrorInvalidValue;
+    return kFns[idx].launch(a, b, c, p, grid, stream, pdl);
 }
 
 cudaError_t variant_max_active(int idx, int* out)
 {
-    switch (idx) {
-    case 0: return max_active_one<1, 256, 4>(out);
-    case 1: return max_active_one<1, 128, 6>(out);
-    case 2: return max_active_one<2, 256, 6>(out);
-    case 3: return max_active_one<2, 128, 8>(out);
-    default: return cudaErrorInvalidValue;
-    }
+    if (idx < 0 || idx >= kNumVariants)
+        return cudaErrorInvalidValue;
+    return kFns[idx].max_active(out);
 }
 
 }  // namespace bwgemm

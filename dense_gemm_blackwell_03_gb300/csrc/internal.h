@@ -11,24 +11,24 @@
 
 namespace bwgemm {
 
-// Compiled kernel variants: (CTA group, BN, ring stages).  Every variant keeps
-// the ring at 192 KiB of shared memory plus 16 KiB of epilogue staging.
+// Compiled kernel variants: (CTA group, BN, ring stages, swapped operands).
+// Every variant keeps the ring at <= 192 KiB of shared memory plus 32 KiB of
+// epilogue staging.  The swapped variants compute C^T = B A^T for small M.
 struct Variant {
     int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
-    int bn;      // columns of C per unit (= MMA N)
+    int bn;      // columns of the MMA per unit (= MMA N)
     int stages;  // shared-memory ring depth
+    bool trans;  // operands swapped, accumulator holds C transposed
 };
 
 constexpr Variant kVariants[] = {
-    {1, 256, 4},
-    {1, 128, 6},
-    {2, 256, 6},
-    {2, 128, 8},
+    {1, 256, 4, false}, {1, 128, 6, false}, {2, 256, 6, false}, {2, 128, 8, false},
+    {2, 128, 8, true},  {2, 64, 9, true},   {1, 128, 6, true},  {1, 64, 8, true},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
 // Index into kVariants, or -1.
-int find_variant(int cg, int bn);
+int find_variant(int cg, int bn, bool trans);
 
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);
@@ -49,6 +49,7 @@ constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) a
 struct Selection {
     bwgemm_config_t cfg;
     int variant_idx;
+    bool swap;  // the kernel sees the problem N x M (A and B exchanged)
     int num_m_blocks, num_n_blocks, num_k_blocks;
     int64_t sk_iters;
 };

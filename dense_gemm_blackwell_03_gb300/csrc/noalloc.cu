@@ -99,7 +99,7 @@ bwgemm_status_t setup_device(int dev, DeviceSetup** out)
             return BWGEMM_ERR_CUDA;
         }
         int pairs = 0;
-        if (variant_max_active(find_variant(2, 256), &pairs) != cudaSuccess || pairs <= 0) {
+        if (variant_max_active(find_variant(2, 256, false), &pairs) != cudaSuccess || pairs <= 0) {
             cudaGetLastError();
             return BWGEMM_ERR_UNSUPPORTED;
         }
@@ -145,6 +145,7 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     bwgemm_plan_options_t opts;
     bwgemm_default_options(&opts);
     opts.split_k = split_k;
+    opts.swap_ab = 1;  // operands in the order given
     Selection sel;
     // plan as if the workspace were unbounded, then hold the need against the array
     if ((st = select_config(ds->num_sms, ds->max_pairs, M, N, K, opts, ~uint64_t(0), &sel)) != BWGEMM_OK)

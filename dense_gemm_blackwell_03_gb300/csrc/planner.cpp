@@ -29,23 +29,38 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
         if (r != 0)
             return BWGEMM_ERR_INVALID_ARG;
 
+    // Operand order.  For a small-M, wide-N problem (decode batches of <= 64
+    // rows) the kernel computes C^T = B A^T: B's N rows fill the 128-row MMA
+    // side and A's few rows become a 64-wide MMA N, so a pipeline stage is
+    // two thirds weights instead of padding.  (At M = 256 swapping doubles
+    // the weight traffic into the SMs and measured slower.)
+    bool swap;
+    switch (opts.swap_ab) {
+    case 0: swap = (M <= 64 && N >= 1024); break;
+    case 1: swap = false; break;
+    case 2: swap = true; break;
+    default: return BWGEMM_ERR_INVALID_ARG;
+    }
+    const int64_t Mk = swap ? N : M;  // the kernel's M and N
+    const int64_t Nk = swap ? M : N;
+
     // Variant: the CTA-pair form (256-row units, each CTA streaming half of the
     // B tile) whenever there are more than 128 rows; one CTA per unit otherwise.
     int cg;
     switch (opts.variant) {
-    case BWGEMM_VARIANT_AUTO: cg = (M > 128) ? 2 : 1; break;
+    case BWGEMM_VARIANT_AUTO: cg = (Mk > 128 && !swap) ? 2 : 1; break;
     case BWGEMM_VARIANT_1SM: cg = 1; break;
     case BWGEMM_VARIANT_2SM: cg = 2; break;
     default: return BWGEMM_ERR_INVALID_ARG;
     }
     int bn;
-    switch (opts.tile_n) {
-    case 0: bn = (N <= 128) ? 128 : 256; break;
-    case 128:
-    case 256: bn = opts.tile_n; break;
-    default: return BWGEMM_ERR_INVALID_ARG;
-    }
-    const int idx = find_variant(cg, bn);
+    if (opts.tile_n == 0)
+        bn = swap ? (Nk <= 64 ? 64 : 128) : (Nk <= 128 ? 128 : 256);
+    else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 256)
+        bn = opts.tile_n;
+    else
+        return BWGEMM_ERR_INVALID_ARG;
+    const int idx = find_variant(cg, bn, swap);
     if (idx < 0)
         return BWGEMM_ERR_UNSUPPORTED;
     if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0 || opts.prefetch < -1 ||
@@ -53,8 +68,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
         return BWGEMM_ERR_INVALID_ARG;
 
     const int tile_m = kRowsPerCta * cg;
-    const int64_t num_m = ceil_div(M, tile_m);
-    const int64_t num_n = ceil_div(N, bn);
+    const int64_t num_m = ceil_div(Mk, tile_m);
+    const int64_t num_n = ceil_div(Nk, bn);
     const int64_t num_kb = ceil_div(K, kTileK);
     const int64_t tiles = num_m * num_n;
     if (num_m > (1 << 30) || num_n > (1 << 30) || tiles > (int64_t(1) << 30))
@@ -145,6 +160,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     Selection sel;
     std::memset(&sel, 0, sizeof(sel));
     sel.variant_idx = idx;
+    sel.swap = swap;
     sel.num_m_blocks = int(num_m);
     sel.num_n_blocks = int(num_n);
     sel.num_k_blocks = int(num_kb);
@@ -165,6 +181,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.cfg.sk_tiles = int32_t(sk_tiles);
     sel.cfg.workers = int32_t(workers);
     sel.cfg.split_scatter = scatter ? 1 : 0;
+    sel.cfg.swap_ab = swap ? 1 : 0;
     *out = sel;
     return BWGEMM_OK;
 }
@@ -174,8 +191,8 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
     const Variant& v = kVariants[sel.variant_idx];
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    p.M = int32_t(M);
-    p.N = int32_t(N);
+    p.M = int32_t(sel.swap ? N : M);  // the kernel's problem
+    p.N = int32_t(sel.swap ? M : N);
     p.K = int32_t(K);
     p.num_m_blocks = sel.num_m_blocks;
     p.num_n_blocks = sel.num_n_blocks;

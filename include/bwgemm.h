@@ -75,7 +75,7 @@ typedef enum {
  * defaults with bwgemm_default_options(). */
 typedef struct {
     int32_t variant;          /* bwgemm_variant_t                                       */
-    int32_t tile_n;           /* 0, 128 or 256: columns of C per work unit              */
+    int32_t tile_n;           /* 0 = auto, 64, 128 or 256: MMA N per work unit          */
     int32_t split_k;          /* 0 = auto, 1 = off, s >= 2: s K-slices per tile         */
     int32_t raster_group;     /* 0 = auto; m-blocks walked before stepping along N      */
     int32_t max_ctas;         /* 0 = fill the GPU; else cap on the persistent grid      */
@@ -90,7 +90,9 @@ typedef struct {
                                  (read back with bwgemm_plan_read_trace)                */
     int32_t prefetch;         /* K blocks of A and B prefetched into L2 ahead of the
                                  shared-memory loads: 0 = default (none), -1 = none     */
-    int32_t reserved[4];      /* must be zero                                            */
+    int32_t swap_ab;          /* 0 = auto, 1 = never, 2 = always: compute C^T = B A^T so
+                                 that B's rows fill the 128-row MMA side (small M)       */
+    int32_t reserved[3];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -112,7 +114,8 @@ typedef struct {
     int32_t workers;      /* CTAs or CTA pairs of the persistent grid            */
     int32_t split_scatter; /* 1: the split_k slices of each tile run in one wave
                               and reduce-scatter their partials                  */
-    int32_t reserved;
+    int32_t swap_ab;      /* 1: operands swapped (tiles over C^T: tile_m along N,
+                             tile_n along M)                                     */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

@@ -49,7 +49,7 @@ def test_struct_layout_matches_header(tmp_path):
         '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(bwgemm_plan_options_t), '
         "offsetof(bwgemm_plan_options_t, timeout_ns), offsetof(bwgemm_plan_options_t, pdl_off), "
         "sizeof(bwgemm_config_t), offsetof(bwgemm_config_t, workspace_bytes), "
-        "offsetof(bwgemm_config_t, split_scatter));\n"
+        "offsetof(bwgemm_config_t, swap_ab));\n"
         "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
@@ -58,7 +58,7 @@ def test_struct_layout_matches_header(tmp_path):
                                           text=True).stdout.split()]
     assert got == [ctypes.sizeof(PlanOptions), PlanOptions.timeout_ns.offset,
                    PlanOptions.pdl_off.offset, ctypes.sizeof(Config), Config.workspace_bytes.offset,
-                   Config.split_scatter.offset]
+                   Config.swap_ab.offset]
 
 
 def test_version_and_status_strings(lib):
@@ -130,7 +130,7 @@ def test_select_even_waves_stay_whole_tiles():
 
 
 def test_select_small_m_splits_k_in_one_wave():
-    c = cfg(64, 8192, 8192, sms=152, pairs=76)
+    c = cfg(64, 8192, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["variant"] == 1 and c["tile_m"] == 128 and c["num_tiles"] == 32
     # fewer tiles than SMs: 4 K slices per tile, all 128 slices in one wave,
     # reduce-scattering their partials
@@ -141,27 +141,48 @@ def test_select_small_m_splits_k_in_one_wave():
 def test_select_decode_shapes():
     # attention out / MLP down: 32 tiles of 256 x 256 over 76 pairs -> 2 slices each
     for N, K in ((8192, 8192), (8192, 28672)):
-        c = cfg(256, N, K, sms=152, pairs=76)
+        c = cfg(256, N, K, sms=152, pairs=76, swap_ab=1)
         assert c["variant"] == 2 and c["num_tiles"] == 32 and c["split_k"] == 2
         assert c["split_scatter"] == 1 and c["grid"] == 128
     # fused QKV: 40 tiles, 2 slices would not fit one wave -> stream-K over all pairs
-    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
     # MLP up: 112 tiles = 1.47 waves -> stream-K
-    c = cfg(256, 28672, 8192, sms=152, pairs=76)
+    c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["dp_tiles"] == 0
     # Gemma-like 512 x 8192 x 5376: 64 tiles fill 84 % of the pairs -> whole tiles
     c = cfg(512, 8192, 5376, sms=152, pairs=76)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 128
 
 
+def test_select_swapped_operands_for_small_m():
+    # M <= 64 decode: C^T = B A^T, 128 rows of B per CTA, A's rows as a 64-wide
+    # MMA N; 64 tiles, two K slices each, all in one wave
+    for M in (1, 16, 64):
+        c = cfg(M, 8192, 8192, sms=152, pairs=76)
+        assert c["swap_ab"] == 1 and c["variant"] == 1 and (c["tile_m"], c["tile_n"]) == (128, 64)
+        assert c["num_tiles"] == 64 and c["split_k"] == 2 and c["split_scatter"] == 1
+        assert c["grid"] == 128
+    # larger M or narrow N keep the operand order
+    assert cfg(256, 8192, 8192)["swap_ab"] == 0
+    assert cfg(512, 8192, 5376)["swap_ab"] == 0
+    assert cfg(64, 512, 4096)["swap_ab"] == 0
+    # forced either way; 256-wide units do not exist in swapped form
+    c = cfg(256, 8192, 8192, swap_ab=2)
+    assert c["swap_ab"] == 1 and c["tile_n"] == 128
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 8192, 8192, swap_ab=2, tile_n=256)
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 8192, 8192, swap_ab=3)
+
+
 def test_select_tiles_schedule_splits_k():
-    c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES)
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2
     assert c["num_units"] == 64 and c["grid"] == 128 and c["split_scatter"] == 1
     assert c["workspace_bytes"] == (1 << 20) + 32 * 2 * 2 * 128 * 256 * 4
     # more slices than one wave holds: no reduce-scatter (slices may not wait)
-    c = cfg(256, 8192, 8192, sms=152, pairs=76, split_k=3)
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, split_k=3, swap_ab=1)
     assert c["split_k"] == 3 and c["split_scatter"] == 0
 
 
@@ -194,7 +215,7 @@ def test_select_rejects_bad_options():
     with pytest.raises(binding.BwgemmError):
         cfg(512, 512, 512, variant=7)
     with pytest.raises(binding.BwgemmError) as e:
-        cfg(256, 8192, 8192, split_k=4, workspace_bytes=1 << 20)
+        cfg(256, 8192, 8192, split_k=4, workspace_bytes=1 << 20, swap_ab=1)
     assert e.value.status == WORKSPACE
     with pytest.raises(binding.BwgemmError) as e:
         cfg(4096, 4096, 4096, schedule=binding.SCHEDULE_STREAM_K, workspace_bytes=1 << 20)

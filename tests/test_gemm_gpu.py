@@ -129,6 +129,35 @@ def test_split_k_reduce_scatter_and_multi_wave(variant, split, max_ctas):
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("variant,tile_n", [(1, 64), (1, 128), (2, 64), (2, 128)])
+@pytest.mark.parametrize("M,N,K,opts", [
+    (1, 1000, 520, {}),                          # one row of A, ragged N and K
+    (37, 2056, 1040, {}),                         # ragged everything
+    (200, 1536, 2048, {"split_k": 2}),            # one-wave split-K on swapped tiles
+    (64, 4096, 4096, {"schedule": 2}),            # stream-K on swapped tiles
+    (130, 3072, 1024, {"split_k": 3, "max_ctas": 4}),  # multi-wave split-K
+])
+def test_swapped_operands_exact(variant, tile_n, M, N, K, opts):
+    # C^T = B A^T on the tensor cores, each accumulator box stored transposed
+    A = make_matrix(M, K, "int2", seed=1900 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=2000 + N, device="cuda")
+    with binding.Plan(0, variant=variant, tile_n=tile_n, swap_ab=2, **opts) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["swap_ab"] == 1 and c["tile_n"] == tile_n
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_swapped_operands_normal_inputs(dtype):
+    A = make_matrix(96, 4096, "normal", dtype, seed=2100, device="cuda")
+    B = make_matrix(3000, 4096, "weight", dtype, seed=2101, device="cuda")
+    Cbuf = torch.full((96, 3008), 3.0, dtype=TORCH16[dtype], device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, dtype, out=Cbuf[:, :3000])
+        assert p.last_config()["swap_ab"] == 1
+    assert torch.all(Cbuf[:, 3000:] == 3.0)
+
+
 def test_split_k_normal_inputs():
     A = make_matrix(200, 4096, "normal", seed=910, device="cuda")
     B = make_matrix(384, 4096, "weight", seed=911, device="cuda")
@@ -296,3 +325,44 @@ def test_timeline_trace_is_ordered():
                 assert ms <= me
             if es and ee:
                 assert es <= ee
+
+
+@pytest.mark.parametrize("variant,schedule", [(1, 1), (2, 1), (2, 2)])
+def test_bounded_wait_reports_timeout_and_context_survives(variant, schedule):
+    # the producer of CTA 0 never fills K block 1 of its first unit: the MMA's
+    # wait on that stage runs out after timeout_ns, every role leaves its loop,
+    # TMEM is freed and the call reports BWGEMM_ERR_TIMEOUT -- no trap, no hang
+    A = make_matrix(512, 1024, "int2", seed=1700, device="cuda")
+    B = make_matrix(512, 1024, "int2", seed=1701, device="cuda")
+    with binding.Plan(0, variant=variant, schedule=schedule, stall_kblock=1,
+                      timeout_ns=200_000_000) as p:
+        p.gemm(A, B)
+        assert p.status() == 6  # BWGEMM_ERR_TIMEOUT
+        assert p.last_device_status() != 0
+    # the context is still usable and a normal plan gives exact results
+    with binding.Plan(0, variant=variant, schedule=schedule) as p:
+        run_full(p, A, B, "bf16", exact=True)
+
+
+def test_cuda_graph_capture_and_replay():
+    # bwgemm_run enqueues one kernel and allocates nothing, so a stream can
+    # capture it; replays see the operands' current contents
+    A = make_matrix(384, 1024, "int2", seed=1800, device="cuda")
+    B = make_matrix(640, 1024, "int2", seed=1801, device="cuda")
+    C = torch.empty(384, 640, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0) as p:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            p.gemm(A, B, out=C, stream=s)  # warm-up launch outside the capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                p.gemm(A, B, out=C, stream=s)
+        torch.cuda.synchronize()
+        for seed in (1802, 1803):
+            A.copy_(make_matrix(384, 1024, "int2", seed=seed, device="cuda"))
+            C.fill_(0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert p.status() == 0
+            compare(bits_of(C), oracle.gemm(bits_of(A), bits_of(B), "bf16"), "bf16", 1024, exact=True)

@@ -17,6 +17,7 @@ FP16 = 1
 SCHEDULE_AUTO = 0
 SCHEDULE_TILES = 1
 SCHEDULE_STREAM_K = 2
+SCHEDULE_CLC = 3
 
 STATUS_NAMES = {
     0: "BWGEMM_OK",

@@ -65,8 +65,10 @@ struct KernelConfig {
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
-    static constexpr int kNumBars = 2 * STAGES + 4;  // full[S], empty[S], acc_full[2], acc_empty[2]
-    static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+    // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4]
+    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * kClcSlots;
+    static constexpr int kOffClcResp = kOffBar + kNumBars * 8;  // 16-byte responses
+    static constexpr int kOffTmemSlot = kOffClcResp + 16 * kClcSlots;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KiB
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
@@ -189,6 +191,81 @@ __device__ __forceinline__ void trace_unit(const GemmParams& p, int unit, int wh
         p.trace[size_t(blockIdx.x) * kTraceSlots + kTraceUnit0 + 4 * unit + which] =
             ptx::global_timer_ns();
 }
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                           volatile uint32_t* abort_flag, uint32_t code);
+
+// The tile sequence of one worker.  Static: the stream-K / data-parallel
+// iteration above.  With cluster launch control (p.clc): the cluster starts
+// on the tile of its own launch index; every later tile is a cluster whose
+// launch the leader cancelled, announced through a ring of kClcSlots
+// responses (clc_full: response landed; clc_empty, in the leader CTA: every
+// reader of both CTAs has decoded it).
+struct Sched {
+    UnitIter st;
+    bool clc, first;
+    int r;                    // next response to read
+    uint32_t resp, full, empty_leader;
+
+    __device__ __forceinline__ void init(const GemmParams& p, int worker, int workers,
+                                         uint32_t resp0, uint32_t full0, uint32_t empty0_leader)
+    {
+        st.init(p, worker, workers);
+        clc = p.clc != 0;
+        first = true;
+        r = 0;
+        resp = resp0;
+        full = full0;
+        empty_leader = empty0_leader;
+    }
+
+    // Next unit; `arrive`: this thread reports its reading of a response.
+    // WARP: the whole warp calls and decodes; it reconverges before the
+    // arriving lane releases the slot.  `code`: status bit of a timeout.
+    template <int CG, bool WARP = false>
+    __device__ __forceinline__ bool next(const GemmParams& p, WorkUnit& w, bool arrive,
+                                         volatile uint32_t* abort_flag, uint32_t code)
+    {
+        if (!clc)
+            return st.next(p, w);
+        int tile;
+        if (first) {
+            first = false;
+            tile = int(blockIdx.x) / CG;
+        } else {
+            const int slot = r % kClcSlots;
+            const uint32_t parity = uint32_t(r / kClcSlots) & 1u;
+            bool landed = wait_phase(full + 8 * slot, parity, p, abort_flag, code);
+            if constexpr (WARP)
+                landed = __all_sync(0xffffffffu, landed);
+            if (!landed)
+                return false;
+            uint32_t x = 0;
+            const bool ok = ptx::clc_query(resp + 16 * slot, x);
+            if constexpr (WARP)
+                __syncwarp();
+            if (arrive) {
+                if constexpr (CG == 1)
+                    ptx::mbar_arrive(empty_leader + 8 * slot);
+                else
+                    ptx::mbar_arrive_cluster(empty_leader + 8 * slot);
+            }
+            ++r;
+            tile = ok ? int(x) / CG : -1;
+        }
+        if (tile < 0 || tile >= p.num_tiles)
+            return false;
+        w.tile = tile;
+        w.kb0 = 0;
+        w.kb1 = p.num_k_blocks;
+        w.kind = kUnitWhole;
+        w.split = 0;
+        w.sk_tile = 0;
+        w.slot = 0;
+        raster(p, w.tile, w.m_blk, w.n_blk);
+        return true;
+    }
+};
 
 // Bounded wait on an mbarrier phase.  Gives up after p.timeout_ns (recording
 // `code` in the status word) or as soon as another role of this CTA gave up.
@@ -369,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_empty = bar_full + 8 * STAGES;      // + 8 * stage
     const uint32_t bar_acc_full = bar_empty + 8 * STAGES;  // + 8 * buffer
     const uint32_t bar_acc_empty = bar_acc_full + 16;      // + 8 * buffer
+    const uint32_t bar_clc_full = bar_acc_empty + 16;      // + 8 * slot
+    const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots;  // + 8 * slot (leader's counts)
+    const uint32_t clc_resp = base + Cfg::kOffClcResp;     // + 16 * slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
 
@@ -381,6 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_acc_full + 8 * b, 1);                // one tcgen05.commit
             ptx::mbar_init(bar_acc_empty + 8 * b, kEpiWarps * CG);  // every epilogue warp of the pair
+        }
+        for (int s = 0; s < kClcSlots; ++s) {
+            ptx::mbar_init(bar_clc_full + 8 * s, 1);  // local producer's arrive.expect_tx(16)
+            // readers of a response: producers and epilogue warps of both CTAs, the MMA thread
+            ptx::mbar_init(bar_clc_empty + 8 * s, CG * (1 + kEpiWarps) + 1);
         }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -409,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::launch_dependents();
     if (threadIdx.x == 0)
         trace_mark(p, kTraceReady);
+    const uint32_t clc_empty_leader = (CG == 2) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -417,10 +503,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool first_unit = true;
-            UnitIter iter;
-            iter.init(p, worker, workers);
+            int requested = 0;
+            Sched iter;
+            iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
-            while (ok && iter.next(p, w)) {
+            while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusProducerTimeout)) {
+                if (p.clc) {
+                    // ask for the tile after this one now, a whole tile ahead of need
+                    const int rq = requested++;
+                    const int slot = rq % kClcSlots;
+                    if (rank == 0 &&
+                        !wait_phase(bar_clc_empty + 8 * slot, (uint32_t(rq / kClcSlots) & 1u) ^ 1u, p,
+                                    abort_flag, kStatusProducerTimeout)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(bar_clc_full + 8 * slot, 16);
+                    if (rank == 0) {
+                        if constexpr (CG == 1)
+                            ptx::clc_try_cancel(clc_resp + 16 * slot, bar_clc_full + 8 * slot);
+                        else
+                            ptx::clc_try_cancel_all(clc_resp + 16 * slot, bar_clc_full + 8 * slot);
+                    }
+                }
                 const int a_row = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta;
                 const int b_row = w.n_blk * BN + int(rank) * Cfg::kBRows;
                 // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
@@ -480,10 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int t = 0;
             bool ok = true;
-            UnitIter iter;
-            iter.init(p, worker, workers);
+            Sched iter;
+            iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
-            while (ok && iter.next(p, w)) {
+            while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusMmaTimeout)) {
                 const int buf = t & 1;
                 const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
                 ++t;
@@ -541,17 +646,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* const parts = reinterpret_cast<float4*>(p.partials);
         int chunk_ctr = 0;
         int t = 0;
-        UnitIter iter;
-        iter.init(p, worker, workers);
+        Sched iter;
+        iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
         WorkUnit w;
-        while (iter.next(p, w)) {
+        while (iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusEpilogueTimeout)) {
             if (t > 0 && warp == 2 && lane == 0)
                 trace_unit(p, t - 1, 3);  // previous unit's epilogue finished
             const int buf = t & 1;
             const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
             ++t;
-            if (!wait_phase(bar_acc_full + 8 * buf, acc_phase, p, abort_flag,
-                            kStatusEpilogueTimeout))
+            // the warp leaves together: a lane that timed out just as the phase
+            // completed must not strand the others in the aligned TMEM loads
+            if (!__all_sync(0xffffffffu, wait_phase(bar_acc_full + 8 * buf, acc_phase, p, abort_flag,
+                                                    kStatusEpilogueTimeout)))
                 break;
             ptx::tc_fence_after_sync();
             if (warp == 2 && lane == 0)

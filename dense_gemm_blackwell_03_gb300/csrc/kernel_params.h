@@ -20,6 +20,7 @@ constexpr int kRowsPerCta = 128;       // accumulator rows per CTA (TMEM lanes)
 constexpr int kEpiWarps = 8;           // two warps per 32-lane quarter of TMEM, half the columns each
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, 8 epilogue warps
 constexpr int kCountersPerWarp = 1;    // arrival counters per (tile, cta, epilogue warp)
+constexpr int kClcSlots = 4;           // cluster-launch-control responses in flight
 constexpr int kStoreCols = 32;         // columns per epilogue store box (64 B rows)
 
 #ifdef __CUDACC__
@@ -66,7 +67,8 @@ struct GemmParams {
     int32_t stall_kblock;   // test hook: producer never fills this k-block of its first unit (< 0: off)
     int32_t split_scatter;  // split-K in one wave: the slices of a tile reduce-scatter (see epilogue)
     int32_t prefetch;       // K blocks the producer prefetches into L2 ahead of its loads (0: off)
-    int32_t pad_;
+    int32_t clc;            // 1: one cluster per tile, running clusters take over pending ones
+                            //    through cluster launch control (whole tiles only)
     uint64_t* trace;        // optional timeline: kTraceSlots %globaltimer stamps per CTA (null: off)
 };
 

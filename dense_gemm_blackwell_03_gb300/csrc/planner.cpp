@@ -79,8 +79,11 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     int64_t slots = (cg == 2) ? max_pairs : num_sms;
     if (opts.max_ctas > 0)
         slots = std::max<int64_t>(1, std::min<int64_t>(slots, opts.max_ctas / cg));
-    if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_STREAM_K)
+    if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_CLC)
         return BWGEMM_ERR_INVALID_ARG;
+    const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
+    if (clc && opts.split_k > 1)
+        return BWGEMM_ERR_INVALID_ARG;  // cluster launch control hands out whole tiles only
 
     // Schedule.  Whole tiles when they fill the workers evenly.  With fewer
     // tiles than workers: whole tiles when they still occupy >= 80 % of the
@@ -91,7 +94,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     // tiles and the K iterations of the remaining tiles are divided evenly.
     bool stream_k = false;
     int64_t auto_split = 1;
-    if (opts.split_k > 1 || opts.schedule == BWGEMM_SCHEDULE_TILES || tiles == 0) {
+    if (opts.split_k > 1 || opts.schedule == BWGEMM_SCHEDULE_TILES || clc || tiles == 0) {
         stream_k = false;
     } else if (opts.schedule == BWGEMM_SCHEDULE_STREAM_K) {
         stream_k = true;
@@ -132,6 +135,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
         // when the tiles alone leave most workers idle; >= 4 K blocks per slice
         if (opts.split_k > 0) {
             s = std::min<int64_t>(opts.split_k, std::max<int64_t>(num_kb, 1));
+        } else if (clc) {
+            s = 1;
         } else if (auto_split > 1) {
             s = auto_split;
         } else if (opts.schedule == BWGEMM_SCHEDULE_TILES && tiles > 0 && tiles < slots &&
@@ -149,7 +154,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
                 ws = 0;
             }
         }
-        workers = std::min<int64_t>(tiles * s, slots);
+        // with cluster launch control the grid holds one cluster per tile
+        workers = clc ? tiles : std::min<int64_t>(tiles * s, slots);
     }
     // all slices of every tile in one wave: they may wait for one another
     const bool scatter = !stream_k && s > 1 && tiles * s <= slots;
@@ -176,7 +182,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.cfg.num_units = int32_t(dp_tiles * s);
     sel.cfg.grid = int32_t(workers * cg);
     sel.cfg.workspace_bytes = ws;
-    sel.cfg.schedule = stream_k ? BWGEMM_SCHEDULE_STREAM_K : BWGEMM_SCHEDULE_TILES;
+    sel.cfg.schedule = clc ? BWGEMM_SCHEDULE_CLC
+                           : (stream_k ? BWGEMM_SCHEDULE_STREAM_K : BWGEMM_SCHEDULE_TILES);
     sel.cfg.dp_tiles = int32_t(dp_tiles);
     sel.cfg.sk_tiles = int32_t(sk_tiles);
     sel.cfg.workers = int32_t(workers);
@@ -209,6 +216,7 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
     p.stall_kblock = -1;
     p.split_scatter = sel.cfg.split_scatter;
     p.prefetch = 0;  // L2 prefetch ahead of the loads measured slower on every shape
+    p.clc = sel.cfg.schedule == BWGEMM_SCHEDULE_CLC ? 1 : 0;
     return p;
 }
 

@@ -334,6 +334,52 @@ __device__ __forceinline__ void tmem_ld_wait()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// --------------------------------------------------- cluster launch control
+// Ask the hardware to cancel the launch of a not-yet-running cluster of this
+// grid; the 16-byte response (which cluster, or none left) lands in shared
+// memory and completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar)
+{
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Same, with the response written to the same offset in every CTA of the
+// cluster (each CTA's barrier at `bar`'s offset counts the bytes).
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar)
+{
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128"
+        " [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decode a response: true and the first CTA's x index of the cancelled
+// cluster, or false when no cluster was left to cancel.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& ctaid_x)
+{
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p;\n\t"
+        ".reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+        "}"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    ctaid_x = x;
+    return ok != 0;
+}
+
 // ------------------------------------------------------------ misc memory
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)

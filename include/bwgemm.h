@@ -67,8 +67,11 @@ typedef enum {
 typedef enum {
     BWGEMM_SCHEDULE_AUTO = 0,     /* stream-K when whole tiles leave workers idle         */
     BWGEMM_SCHEDULE_TILES = 1,    /* whole tiles, or split_k slices of every tile          */
-    BWGEMM_SCHEDULE_STREAM_K = 2  /* K iterations of the last tiles divided evenly among
+    BWGEMM_SCHEDULE_STREAM_K = 2, /* K iterations of the last tiles divided evenly among
                                      the workers; the earlier full waves as whole tiles    */
+    BWGEMM_SCHEDULE_CLC = 3       /* whole tiles, one cluster per tile in the grid; running
+                                     clusters take over the tiles of clusters not yet
+                                     launched through cluster launch control               */
 } bwgemm_schedule_t;
 
 /* Plan options.  Zero means "choose automatically" for every field; get the
@@ -106,9 +109,10 @@ typedef struct {
     int32_t raster_group; /* m-blocks per raster group                           */
     int32_t num_tiles;    /* output tiles                                        */
     int32_t num_units;    /* whole-tile / split-K units (dp_tiles x split_k)     */
-    int32_t grid;         /* CTAs launched (persistent)                          */
+    int32_t grid;         /* CTAs launched (persistent, or one cluster per tile
+                             with BWGEMM_SCHEDULE_CLC)                           */
     int64_t workspace_bytes; /* partial-tile bytes used by this shape            */
-    int32_t schedule;     /* BWGEMM_SCHEDULE_TILES or BWGEMM_SCHEDULE_STREAM_K   */
+    int32_t schedule;     /* BWGEMM_SCHEDULE_TILES, _STREAM_K or _CLC            */
     int32_t dp_tiles;     /* tiles computed whole (or as split_k slices)         */
     int32_t sk_tiles;     /* tiles whose K iterations are spread by stream-K     */
     int32_t workers;      /* CTAs or CTA pairs of the persistent grid            */

@@ -176,6 +176,19 @@ def test_select_swapped_operands_for_small_m():
         cfg(256, 8192, 8192, swap_ab=3)
 
 
+def test_select_cluster_launch_control():
+    # one cluster per tile in the grid; running clusters cancel pending ones
+    c = cfg(4096, 4096, 4096, sms=152, pairs=76, schedule=binding.SCHEDULE_CLC)
+    assert c["schedule"] == binding.SCHEDULE_CLC and c["split_k"] == 1 and c["sk_tiles"] == 0
+    assert c["num_tiles"] == 256 and c["workers"] == 256 and c["grid"] == 512
+    c = cfg(64, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_CLC)
+    assert c["swap_ab"] == 1 and c["grid"] == c["num_tiles"] == 64
+    with pytest.raises(binding.BwgemmError):
+        cfg(4096, 4096, 4096, schedule=binding.SCHEDULE_CLC, split_k=2)
+    with pytest.raises(binding.BwgemmError):
+        cfg(4096, 4096, 4096, schedule=4)
+
+
 def test_select_tiles_schedule_splits_k():
     c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2
@@ -221,7 +234,7 @@ def test_select_rejects_bad_options():
         cfg(4096, 4096, 4096, schedule=binding.SCHEDULE_STREAM_K, workspace_bytes=1 << 20)
     assert e.value.status == WORKSPACE
     with pytest.raises(binding.BwgemmError):
-        cfg(512, 512, 512, schedule=3)
+        cfg(512, 512, 512, schedule=5)
     # automatic stream-K falls back to whole tiles when the workspace is too small
     assert cfg(4096, 4096, 4096, workspace_bytes=1 << 20)["schedule"] == binding.SCHEDULE_TILES
 

@@ -152,10 +152,33 @@ def test_swapped_operands_normal_inputs(dtype):
     A = make_matrix(96, 4096, "normal", dtype, seed=2100, device="cuda")
     B = make_matrix(3000, 4096, "weight", dtype, seed=2101, device="cuda")
     Cbuf = torch.full((96, 3008), 3.0, dtype=TORCH16[dtype], device="cuda")
-    with binding.Plan(0) as p:
+    with binding.Plan(0, swap_ab=2) as p:  # 96 rows: above the automatic swap bound
         run_full(p, A, B, dtype, out=Cbuf[:, :3000])
         assert p.last_config()["swap_ab"] == 1
     assert torch.all(Cbuf[:, 3000:] == 3.0)
+
+
+@pytest.mark.parametrize("variant,tile_n,swap", [(1, 256, 1), (1, 128, 1), (2, 256, 1),
+                                                 (2, 128, 1), (1, 64, 2), (2, 128, 2)])
+def test_cluster_launch_control_exact(variant, tile_n, swap):
+    # many more tiles than co-resident clusters: most tiles are taken over
+    # from cancelled cluster launches
+    M, N, K = (4096, 2048, 192) if swap == 1 else (40, 16384, 192)
+    A = make_matrix(M, K, "int2", seed=2200 + variant, device="cuda")
+    B = make_matrix(N, K, "int2", seed=2300 + tile_n, device="cuda")
+    with binding.Plan(0, variant=variant, tile_n=tile_n, swap_ab=swap,
+                      schedule=binding.SCHEDULE_CLC) as p:
+        for _ in range(2):
+            run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["schedule"] == binding.SCHEDULE_CLC and c["grid"] == c["num_tiles"] * variant
+
+
+def test_cluster_launch_control_normal_inputs():
+    A = make_matrix(2000, 1000, "normal", seed=2400, device="cuda")
+    B = make_matrix(3000, 1000, "normal", seed=2401, device="cuda")
+    with binding.Plan(0, schedule=binding.SCHEDULE_CLC) as p:
+        run_full(p, A, B, "bf16")
 
 
 def test_split_k_normal_inputs():

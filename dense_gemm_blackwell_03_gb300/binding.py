@@ -67,7 +67,8 @@ class PlanOptions(ctypes.Structure):
         ("trace", ctypes.c_int32),
         ("prefetch", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("multicast", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -90,6 +91,7 @@ class Config(ctypes.Structure):
         ("workers", ctypes.c_int32),
         ("split_scatter", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32),
+        ("multicast", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

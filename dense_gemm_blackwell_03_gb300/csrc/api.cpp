@@ -141,7 +141,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
         return BWGEMM_OK;
     }
     Selection sel;
-    st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256, false)], M, N, K, plan->opts,
+    st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256, false, 1)],
+                       plan->max_active[find_variant(2, 256, false, 2)], M, N, K, plan->opts,
                        plan->workspace_bytes, &sel);
     if (st != BWGEMM_OK)
         return st;
@@ -152,7 +153,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     const void* opB = sel.swap ? A : B;
     const int64_t rowsA = sel.swap ? N : M, rowsB = sel.swap ? M : N;
     const int64_t ldA = sel.swap ? ldb : lda, ldB = sel.swap ? lda : ldb;
-    if ((st = get_tmap(plan->tmaps[0], opA, dtype, K, rowsA, ldA, kTileK, kRowsPerCta,
+    // with A multicast each CTA loads 128 / mc of its rows for all mc pairs
+    if ((st = get_tmap(plan->tmaps[0], opA, dtype, K, rowsA, ldA, kTileK, uint32_t(kRowsPerCta / v.mc),
                        CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK)
         return st;
     if ((st = get_tmap(plan->tmaps[1], opB, dtype, K, rowsB, ldB, kTileK, b_rows,
@@ -165,6 +167,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     GemmParams p = make_params(sel, M, N, K, dtype);
     p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
     p.status = plan->d_status;
+    p.c = static_cast<uint16_t*>(C);
+    p.ldc = ldc;
     p.tile_sems = reinterpret_cast<uint32_t*>(plan->d_workspace);
     p.partials = reinterpret_cast<float*>(plan->d_workspace + kCounterRegionBytes);
     p.stall_kblock = plan->opts.stall_kblock;

@@ -205,12 +205,17 @@ struct Sched {
     UnitIter st;
     bool clc, first;
     int r;                    // next response to read
+    int cs, mc, pair;         // CTAs per cluster, pairs per cluster, this CTA's pair
     uint32_t resp, full, empty_leader;
 
-    __device__ __forceinline__ void init(const GemmParams& p, int worker, int workers,
-                                         uint32_t resp0, uint32_t full0, uint32_t empty0_leader)
+    __device__ __forceinline__ void init(const GemmParams& p, int worker, int workers, int cs_,
+                                         int mc_, int pair_, uint32_t resp0, uint32_t full0,
+                                         uint32_t empty0_leader)
     {
         st.init(p, worker, workers);
+        cs = cs_;
+        mc = mc_;
+        pair = pair_;
         clc = p.clc != 0;
         first = true;
         r = 0;
@@ -222,16 +227,22 @@ struct Sched {
     // Next unit; `arrive`: this thread reports its reading of a response.
     // WARP: the whole warp calls and decodes; it reconverges before the
     // arriving lane releases the slot.  `code`: status bit of a timeout.
+    // With mc pairs per cluster a tile is a group of mc column blocks, pair i
+    // of the cluster computing block mc * n + i.
     template <int CG, bool WARP = false>
     __device__ __forceinline__ bool next(const GemmParams& p, WorkUnit& w, bool arrive,
                                          volatile uint32_t* abort_flag, uint32_t code)
     {
-        if (!clc)
-            return st.next(p, w);
+        if (!clc) {
+            if (!st.next(p, w))
+                return false;
+            w.n_blk = w.n_blk * mc + pair;
+            return true;
+        }
         int tile;
         if (first) {
             first = false;
-            tile = int(blockIdx.x) / CG;
+            tile = int(blockIdx.x) / cs;
         } else {
             const int slot = r % kClcSlots;
             const uint32_t parity = uint32_t(r / kClcSlots) & 1u;
@@ -251,7 +262,7 @@ struct Sched {
                     ptx::mbar_arrive_cluster(empty_leader + 8 * slot);
             }
             ++r;
-            tile = ok ? int(x) / CG : -1;
+            tile = ok ? int(x) / cs : -1;
         }
         if (tile < 0 || tile >= p.num_tiles)
             return false;
@@ -263,6 +274,7 @@ struct Sched {
         w.sk_tile = 0;
         w.slot = 0;
         raster(p, w.tile, w.m_blk, w.n_blk);
+        w.n_blk = w.n_blk * mc + pair;
         return true;
     }
 };
@@ -346,9 +358,10 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi, int dtype)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Hand a fully read TMEM accumulator back to the MMA warp (of the leader CTA).
+// Hand a fully read TMEM accumulator back to the MMA warp (of the pair's
+// leader CTA, cluster rank `leader`).
 template <int CG>
-__device__ __forceinline__ void release_accumulator(uint32_t bar, int lane)
+__device__ __forceinline__ void release_accumulator(uint32_t bar, int lane, uint32_t leader)
 {
     ptx::tc_fence_before_sync();
     __syncwarp();
@@ -356,7 +369,7 @@ __device__ __forceinline__ void release_accumulator(uint32_t bar, int lane)
         if constexpr (CG == 1)
             ptx::mbar_arrive(bar);
         else
-            ptx::mbar_arrive_cluster(ptx::map_to_cta(bar, 0));
+            ptx::mbar_arrive_cluster(ptx::map_to_cta(bar, leader));
     }
 }
 
@@ -369,12 +382,56 @@ __device__ __forceinline__ void release_accumulator(uint32_t bar, int lane)
 // rows are C columns and accumulator columns are C rows.  Two staging buffers
 // per warp alternate; a buffer is reused only after the bulk store issued
 // from it two boxes earlier finished reading.
+//
+// A TMA store clips at the end of a row of C only in whole 16-byte chunks: a
+// box holding the end of a row whose length is not a multiple of 8 elements
+// would also write the chunk's elements past the end, which belong to the
+// caller.  That box is written with plain stores, element by element.
+template <bool TR>
+__device__ __noinline__ void store_box_ragged(const uint32_t (&packed)[16], const GemmParams& p,
+                                              int lane, int col, int m_row)
+{
+    if constexpr (!TR) {
+        // lane = row m_row + lane; values = columns col .. col + 31
+        const int row = m_row + lane;
+        if (row >= p.M)
+            return;
+        uint16_t* dst = p.c + size_t(row) * size_t(p.ldc);
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (col + i < p.N)
+                dst[col + i] = uint16_t((i & 1) ? (packed[i >> 1] >> 16) : (packed[i >> 1] & 0xFFFFu));
+    } else {
+        // lane = column m_row + lane of C; values = rows col .. col + 31
+        const int c_col = m_row + lane;
+        if (c_col >= p.M)
+            return;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (col + i < p.N)
+                p.c[size_t(col + i) * size_t(p.ldc) + size_t(c_col)] =
+                    uint16_t((i & 1) ? (packed[i >> 1] >> 16) : (packed[i >> 1] & 0xFFFFu));
+    }
+}
+
 template <bool TR>
 __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmParams& p,
                                           const CUtensorMap* tmap_c, uint32_t my_store,
                                           int& chunk_ctr, int lane, int col, int m_row)
 {
     constexpr int kBufBytes = 32 * kStoreCols * 2;
+    // the row end of C inside this box, not on a 16-byte boundary
+    const int row_len = TR ? p.M : p.N;
+    const int box_x = TR ? m_row : col;
+    if ((row_len & 7) != 0 && box_x < row_len && box_x + 32 > row_len) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
+        if ((TR ? col : m_row) < (TR ? p.N : p.M))
+            store_box_ragged<TR>(packed, p, lane, col, m_row);
+        return;
+    }
     const uint32_t sb = my_store + uint32_t((chunk_ctr & 1) * kBufBytes);
     if constexpr (!TR) {
         uint32_t packed[16];
@@ -422,12 +479,18 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
     ++chunk_ctr;
 }
 
-template <int CG, int BN, int STAGES, bool TR>
+// MC: CTA pairs per cluster that share each A tile.  Pair i of the cluster
+// computes column block MC * n + i of the tile group (m, n); the CTAs with the
+// same rank in their pair need the same 128 A rows, so each loads 128 / MC of
+// them once from L2 and multicasts them to all MC.
+template <int CG, int BN, int STAGES, bool TR, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
+    static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
+    constexpr int CS = CG * MC;  // CTAs per cluster
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -435,9 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-    const int worker = blockIdx.x / CG;
-    const int workers = gridDim.x / CG;
+    const uint32_t rank = (CS > 1) ? ptx::cluster_ctarank() : 0u;  // in the cluster
+    const uint32_t prank = (CG == 2) ? (rank & 1u) : 0u;            // in the CTA pair
+    const uint32_t pair = rank / CG;                                // pair of the cluster
+    const uint32_t leader = rank - prank;                           // the pair's MMA CTA
+    const int worker = blockIdx.x / CS;
+    const int workers = gridDim.x / CS;
 
     const uint32_t sA = base + Cfg::kOffA;
     const uint32_t sB = base + Cfg::kOffB;
@@ -456,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         trace_mark(p, kTraceEntry);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);   // producer's arrive.expect_tx (+ bytes)
-            ptx::mbar_init(bar_empty + 8 * s, 1);  // one tcgen05.commit
+            ptx::mbar_init(bar_empty + 8 * s, MC);  // one tcgen05.commit per pair reading the stage
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_acc_full + 8 * b, 1);                // one tcgen05.commit
@@ -464,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kClcSlots; ++s) {
             ptx::mbar_init(bar_clc_full + 8 * s, 1);  // local producer's arrive.expect_tx(16)
-            // readers of a response: producers and epilogue warps of both CTAs, the MMA thread
-            ptx::mbar_init(bar_clc_empty + 8 * s, CG * (1 + kEpiWarps) + 1);
+            // readers of a response: producers and epilogue warps of every CTA, the MMA threads
+            ptx::mbar_init(bar_clc_empty + 8 * s, CS * (1 + kEpiWarps) + MC);
         }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -480,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before_sync();
-    if constexpr (CG == 2)
+    if constexpr (CS > 1)
         ptx::cluster_sync();
     else
         __syncthreads();
@@ -494,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::launch_dependents();
     if (threadIdx.x == 0)
         trace_mark(p, kTraceReady);
-    const uint32_t clc_empty_leader = (CG == 2) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
+    const uint32_t clc_empty_leader = (CS > 1) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -505,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool first_unit = true;
             int requested = 0;
             Sched iter;
-            iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
+            iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
             while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusProducerTimeout)) {
                 if (p.clc) {
@@ -520,14 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mbar_arrive_expect_tx(bar_clc_full + 8 * slot, 16);
                     if (rank == 0) {
-                        if constexpr (CG == 1)
+                        if constexpr (CS == 1)
                             ptx::clc_try_cancel(clc_resp + 16 * slot, bar_clc_full + 8 * slot);
                         else
                             ptx::clc_try_cancel_all(clc_resp + 16 * slot, bar_clc_full + 8 * slot);
                     }
                 }
-                const int a_row = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta;
-                const int b_row = w.n_blk * BN + int(rank) * Cfg::kBRows;
+                const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
+                const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
                 // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
                 // ring only has to cover L2 latency, not DRAM latency
                 const int pf = p.prefetch;
@@ -558,11 +624,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::tma_load_2d(dA, &tmap_a, fb, kb * kTileK, a_row);
                             ptx::tma_load_2d(dB, &tmap_b, fb, kb * kTileK, b_row);
                         } else {
-                            // both CTAs' bytes are counted on the leader's barrier
-                            const uint32_t leader_fb = ptx::map_to_cta(fb, 0);
-                            if (rank == 0)
+                            // both CTAs' bytes are counted on the pair leader's barrier
+                            const uint32_t leader_fb = ptx::map_to_cta(fb, leader);
+                            if (prank == 0)
                                 ptx::mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                            ptx::tma_load_2d_pair(dA, &tmap_a, leader_fb, kb * kTileK, a_row);
+                            if constexpr (MC == 1) {
+                                ptx::tma_load_2d_pair(dA, &tmap_a, leader_fb, kb * kTileK, a_row);
+                            } else {
+                                // rows [pair * 128 / MC, +128 / MC) of this CTA's 128, into
+                                // the same place in every CTA of the cluster with this prank
+                                constexpr int kPart = kRowsPerCta / MC;
+                                uint16_t mask = 0;
+#pragma unroll
+                                for (int i = 0; i < MC; ++i)
+                                    mask |= uint16_t(1u << (int(prank) + CG * i));
+                                ptx::tma_load_2d_pair_multicast(
+                                    dA + uint32_t(pair) * uint32_t(kPart * kTileK * 2), &tmap_a, leader_fb,
+                                    kb * kTileK, a_row + int(pair) * kPart, mask);
+                            }
                             ptx::tma_load_2d_pair(dB, &tmap_b, leader_fb, kb * kTileK, b_row);
                         }
                     }
@@ -577,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0 && rank == 0) {
+        if (lane == 0 && prank == 0) {
             const uint32_t idesc = p.idesc;
             const uint64_t a_desc0 = make_sdesc_sw128(sA);
             const uint64_t b_desc0 = make_sdesc_sw128(sB);
@@ -586,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = 0;
             bool ok = true;
             Sched iter;
-            iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
+            iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
             while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusMmaTimeout)) {
                 const int buf = t & 1;
@@ -612,10 +691,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_f16<CG>(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc,
                                          (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
+                    // the stage is free once every pair sharing it has read it
                     if constexpr (CG == 1)
                         ptx::mma_commit(bar_empty + 8 * stage);
                     else
-                        ptx::mma_commit_pair(bar_empty + 8 * stage, 0x3);
+                        ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t((1u << CS) - 1u));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -626,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (CG == 1)
                     ptx::mma_commit(bar_acc_full + 8 * buf);
                 else
-                    ptx::mma_commit_pair(bar_acc_full + 8 * buf, 0x3);
+                    ptx::mma_commit_pair(bar_acc_full + 8 * buf, uint16_t(0x3u << (CG * pair)));
                 trace_unit(p, t - 1, 1);
             }
         }
@@ -647,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int chunk_ctr = 0;
         int t = 0;
         Sched iter;
-        iter.init(p, worker, workers, clc_resp, bar_clc_full, clc_empty_leader);
+        iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
         WorkUnit w;
         while (iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusEpilogueTimeout)) {
             if (t > 0 && warp == 2 && lane == 0)
@@ -664,13 +744,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 2 && lane == 0)
                 trace_unit(p, t - 1, 2);
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
-            const int cta_row0 = w.m_blk * Cfg::kTileM + int(rank) * kRowsPerCta;
+            const int cta_row0 = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
             const int m_row = cta_row0 + q * 32;  // first row of this warp's boxes
             const int n_col = w.n_blk * BN;
             if (m_row >= p.M) {
                 // every row of this warp is padding past M: nothing to load or store
                 // (the same holds for every piece of the tile, so no counter is used)
-                release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                 continue;
             }
             if (w.kind == kUnitWhole) {
@@ -681,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                     ptx::tmem_ld_wait();
                     if (c == c_end - 1)
-                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                     store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
                 }
                 continue;
@@ -696,11 +776,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // order -- its own share straight from TMEM -- and stores C.
                 const int S = p.split_k;
                 const int j = w.split;
-                const int ctile = w.tile * CG + int(rank);
+                const int ctile = w.tile * CS + int(rank);
                 uint32_t* const cnt = p.tile_sems + size_t(ctile * kEpiWarps + ew) * kCountersPerWarp;
                 const bool row_ok = (cta_row0 + row) < p.M;
                 auto chunk_ptr = [&](int slice, int c) -> float4* {
-                    const size_t slot = size_t(w.tile * S + slice) * CG + rank;
+                    const size_t slot = size_t(w.tile * S + slice) * CS + rank;
                     return parts + slot * kSlotF4 + size_t(c) * 8 * kRowsPerCta + row;
                 };
                 // store the chunks other slices own
@@ -726,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!owns_any)
-                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                 // publish: the warp barrier orders every lane's stores before lane
                 // 0's release-add; the slice that arrives last need not poll
                 __syncwarp();
@@ -781,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::tmem_ld_wait();
                         if (c == last_owned)
-                            release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                            release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
                             r[4 * v + 0] = __float_as_uint(acc[v].x);
@@ -813,20 +893,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (w.kind == kUnitSplit) {
                 pieces = p.split_k;
                 j = w.split;
-                ctile = w.tile * CG + int(rank);
+                ctile = w.tile * CS + int(rank);
             } else {
                 tile_it0 = (long long)w.sk_tile * p.num_k_blocks;
                 first_worker = sk_owner(p, tile_it0, workers);
                 pieces = sk_owner(p, tile_it0 + p.num_k_blocks - 1, workers) - first_worker + 1;
                 j = worker - first_worker;
-                ctile = w.sk_tile * CG + int(rank);
+                ctile = w.sk_tile * CS + int(rank);
             }
             auto slot_of = [&](int i) -> size_t {  // CTA partial slot of piece i
                 if (w.kind == kUnitSplit)
-                    return size_t(w.tile * p.split_k + i) * CG + rank;
+                    return size_t(w.tile * p.split_k + i) * CS + rank;
                 const int wi = first_worker + i;
                 const int si = (sk_begin(p, wi, workers) >= tile_it0) ? 0 : 1;
-                return size_t(wi * 2 + si) * CG + rank;
+                return size_t(wi * 2 + si) * CS + rank;
             };
             uint32_t* const cnt = p.tile_sems + size_t(ctile * kEpiWarps + ew) * kCountersPerWarp;
             const bool row_ok = (cta_row0 + row) < p.M;  // padding rows move no bytes
@@ -853,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ready = wait_counter(cnt, uint32_t(pieces - 1), p, abort_flag);
                 ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                 if (!ready) {
-                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                     continue;
                 }
                 __threadfence();
@@ -888,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                     ptx::tmem_ld_wait();
                     if (c == c_end - 1)
-                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + sp[v].x);
@@ -912,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                 ptx::tmem_ld_wait();
                 if (c == c_end - 1)
-                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane);
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                 if (row_ok) {
                     float4* dst = chunk_ptr(mine, c);
 #pragma unroll
@@ -939,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------------- teardown
     __syncwarp();
     ptx::tc_fence_before_sync();
-    if constexpr (CG == 2)
+    if constexpr (CS > 1)
         ptx::cluster_sync();
     else
         __syncthreads();

@@ -6,12 +6,12 @@ namespace bwgemm {
 
 namespace {
 
-template <int CG, int BN, int STAGES, bool TR>
+template <int CG, int BN, int STAGES, bool TR, int MC>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -23,9 +23,9 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
-    if (CG == 2) {
+    if (CG * MC > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.x = CG * MC;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
@@ -40,16 +40,16 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     return cudaLaunchKernelEx(&cfg, kernel, a, b, c, p);
 }
 
-template <int CG, int BN, int STAGES, bool TR>
+template <int CG, int BN, int STAGES, bool TR, int MC>
 cudaError_t max_active_one(int* out)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    if (CG == 1) {
+    if (CG * MC == 1) {
         int per_sm = 0, dev = 0, sms = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads,
                                                             Cfg::kSmemBytes);
@@ -63,12 +63,12 @@ cudaError_t max_active_one(int* out)
         return cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(CG * MC, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CG * MC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -83,25 +83,28 @@ struct VariantFns {
     int smem_bytes;
 };
 
-#define BWGEMM_VARIANT(CG, BN, ST, TR) \
-    {&launch_one<CG, BN, ST, TR>, &max_active_one<CG, BN, ST, TR>, KernelConfig<CG, BN, ST>::kSmemBytes}
+#define BWGEMM_VARIANT(CG, BN, ST, TR, MC)                                  \
+    {&launch_one<CG, BN, ST, TR, MC>, &max_active_one<CG, BN, ST, TR, MC>, \
+     KernelConfig<CG, BN, ST>::kSmemBytes}
 
 // same order as kVariants in internal.h
 constexpr VariantFns kFns[] = {
-    BWGEMM_VARIANT(1, 256, 4, false), BWGEMM_VARIANT(1, 128, 6, false),
-    BWGEMM_VARIANT(2, 256, 6, false), BWGEMM_VARIANT(2, 128, 8, false),
-    BWGEMM_VARIANT(2, 128, 8, true),  BWGEMM_VARIANT(2, 64, 9, true),
-    BWGEMM_VARIANT(1, 128, 6, true),  BWGEMM_VARIANT(1, 64, 8, true),
+    BWGEMM_VARIANT(1, 256, 4, false, 1), BWGEMM_VARIANT(1, 128, 6, false, 1),
+    BWGEMM_VARIANT(2, 256, 6, false, 1), BWGEMM_VARIANT(2, 128, 8, false, 1),
+    BWGEMM_VARIANT(2, 128, 8, true, 1),  BWGEMM_VARIANT(2, 64, 9, true, 1),
+    BWGEMM_VARIANT(1, 128, 6, true, 1),  BWGEMM_VARIANT(1, 64, 8, true, 1),
+    BWGEMM_VARIANT(2, 256, 6, false, 2), BWGEMM_VARIANT(2, 128, 8, false, 2),
 };
 #undef BWGEMM_VARIANT
 static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");
 
 }  // namespace
 
-int find_variant(int cg, int bn, bool trans)
+int find_variant(int cg, int bn, bool trans, int mc)
 {
     for (int i = 0; i < kNumVariants; ++i)
-        if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans)
+        if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans &&
+            kVariants[i].mc == mc)
             return i;
     return -1;
 }

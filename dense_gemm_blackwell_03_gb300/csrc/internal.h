@@ -11,24 +11,28 @@
 
 namespace bwgemm {
 
-// Compiled kernel variants: (CTA group, BN, ring stages, swapped operands).
-// Every variant keeps the ring at <= 192 KiB of shared memory plus 32 KiB of
-// epilogue staging.  The swapped variants compute C^T = B A^T for small M.
+// Compiled kernel variants: (CTA group, BN, ring stages, swapped operands,
+// pairs per cluster sharing A).  Every variant keeps the ring at <= 192 KiB of
+// shared memory plus 32 KiB of epilogue staging.  The swapped variants
+// compute C^T = B A^T for small M; the mc = 2 variants run clusters of two
+// CTA pairs on adjacent column blocks that multicast their common A tile.
 struct Variant {
     int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
     int bn;      // columns of the MMA per unit (= MMA N)
     int stages;  // shared-memory ring depth
     bool trans;  // operands swapped, accumulator holds C transposed
+    int mc;      // CTA pairs per cluster sharing each A tile (1 = no multicast)
 };
 
 constexpr Variant kVariants[] = {
-    {1, 256, 4, false}, {1, 128, 6, false}, {2, 256, 6, false}, {2, 128, 8, false},
-    {2, 128, 8, true},  {2, 64, 9, true},   {1, 128, 6, true},  {1, 64, 8, true},
+    {1, 256, 4, false, 1}, {1, 128, 6, false, 1}, {2, 256, 6, false, 1}, {2, 128, 8, false, 1},
+    {2, 128, 8, true, 1},  {2, 64, 9, true, 1},   {1, 128, 6, true, 1},  {1, 64, 8, true, 1},
+    {2, 256, 6, false, 2}, {2, 128, 8, false, 2},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
 // Index into kVariants, or -1.
-int find_variant(int cg, int bn, bool trans);
+int find_variant(int cg, int bn, bool trans, int mc = 1);
 
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);
@@ -39,8 +43,8 @@ int variant_smem_bytes(int idx);
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
-// Co-resident clusters (CTA pairs for cg == 2, CTAs for cg == 1) of variant
-// `idx` on the current device.
+// Co-resident clusters (of cg * mc CTAs; single CTAs for cg * mc == 1) of
+// variant `idx` on the current device.
 cudaError_t variant_max_active(int idx, int* out);
 
 // Sizes of the split-K workspace regions.
@@ -59,7 +63,8 @@ struct Selection {
 GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype);
 
 // Host-only configuration choice (also behind bwgemm_select_config).
-bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, int64_t K,
+// max_pairs / max_quads: co-resident clusters of 2 and of 4 CTAs.
+bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t M, int64_t N, int64_t K,
                               const bwgemm_plan_options_t& opts, uint64_t workspace_bytes,
                               Selection* out);
 

@@ -70,6 +70,8 @@ struct GemmParams {
     int32_t clc;            // 1: one cluster per tile, running clusters take over pending ones
                             //    through cluster launch control (whole tiles only)
     uint64_t* trace;        // optional timeline: kTraceSlots %globaltimer stamps per CTA (null: off)
+    uint16_t* c;            // C itself, for the boxes a TMA store cannot clip exactly
+    int64_t ldc;            // elements between rows of C
 };
 
 // Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).

@@ -99,7 +99,7 @@ bwgemm_status_t setup_device(int dev, DeviceSetup** out)
             return BWGEMM_ERR_CUDA;
         }
         int pairs = 0;
-        if (variant_max_active(find_variant(2, 256, false), &pairs) != cudaSuccess || pairs <= 0) {
+        if (variant_max_active(find_variant(2, 256, false, 1), &pairs) != cudaSuccess || pairs <= 0) {
             cudaGetLastError();
             return BWGEMM_ERR_UNSUPPORTED;
         }
@@ -145,10 +145,12 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     bwgemm_plan_options_t opts;
     bwgemm_default_options(&opts);
     opts.split_k = split_k;
-    opts.swap_ab = 1;  // operands in the order given
+    opts.swap_ab = 1;    // operands in the order given
+    opts.multicast = 1;  // one CTA pair per cluster: the scratch below is sized for it
     Selection sel;
     // plan as if the workspace were unbounded, then hold the need against the array
-    if ((st = select_config(ds->num_sms, ds->max_pairs, M, N, K, opts, ~uint64_t(0), &sel)) != BWGEMM_OK)
+    if ((st = select_config(ds->num_sms, ds->max_pairs, 0, M, N, K, opts, ~uint64_t(0), &sel)) !=
+        BWGEMM_OK)
         return st;
     const Variant& v = kVariants[sel.variant_idx];
     const int S = sel.cfg.split_k;
@@ -177,6 +179,8 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     GemmParams p = make_params(sel, M, N, K, dtype);
     p.timeout_ns = 4000000000ull;
     p.status = status;
+    p.c = static_cast<uint16_t*>(C);
+    p.ldc = ldc;
     p.tile_sems = ctr;
     p.partials = reinterpret_cast<float*>(partials);
     return launch_variant(sel.variant_idx, ta, tb, tc, p, sel.cfg.grid, s, false) == cudaSuccess

@@ -17,14 +17,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, int64_t K,
-                              const bwgemm_plan_options_t& opts, uint64_t workspace_bytes,
-                              Selection* out)
+bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t M, int64_t N,
+                              int64_t K, const bwgemm_plan_options_t& opts,
+                              uint64_t workspace_bytes, Selection* out)
 {
     if (!out || num_sms <= 0 || M < 0 || N < 0 || K < 0)
         return BWGEMM_ERR_INVALID_ARG;
     if (max_pairs <= 0)
         max_pairs = num_sms / 2;
+    if (max_quads <= 0)
+        max_quads = std::max(1, max_pairs / 2);
     for (int32_t r : opts.reserved)
         if (r != 0)
             return BWGEMM_ERR_INVALID_ARG;
@@ -60,7 +62,20 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
         bn = opts.tile_n;
     else
         return BWGEMM_ERR_INVALID_ARG;
-    const int idx = find_variant(cg, bn, swap);
+    // A multicast: clusters of two CTA pairs on adjacent column blocks, each
+    // A tile read from L2 once for both pairs.  Off unless asked for: only 36
+    // clusters of 4 CTAs fit on the 152 SMs at once (144 SMs), and the ~4 %
+    // it gains per SM (8192^3) does not make up for the 8 idle SMs.
+    int mc;
+    switch (opts.multicast) {
+    case 0: mc = 1; break;
+    case 1: mc = 1; break;
+    case 2: mc = 2; break;
+    default: return BWGEMM_ERR_INVALID_ARG;
+    }
+    if (mc > 1 && (cg != 2 || swap))
+        return BWGEMM_ERR_UNSUPPORTED;
+    const int idx = find_variant(cg, bn, swap, mc);
     if (idx < 0)
         return BWGEMM_ERR_UNSUPPORTED;
     if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0 || opts.prefetch < -1 ||
@@ -69,16 +84,18 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
 
     const int tile_m = kRowsPerCta * cg;
     const int64_t num_m = ceil_div(Mk, tile_m);
-    const int64_t num_n = ceil_div(Nk, bn);
+    const int64_t num_n = ceil_div(Nk, int64_t(bn) * mc);  // column groups of mc blocks
     const int64_t num_kb = ceil_div(K, kTileK);
     const int64_t tiles = num_m * num_n;
     if (num_m > (1 << 30) || num_n > (1 << 30) || tiles > (int64_t(1) << 30))
         return BWGEMM_ERR_UNSUPPORTED;
 
-    // Workers (CTA pairs, or CTAs) the persistent grid holds at once.
-    int64_t slots = (cg == 2) ? max_pairs : num_sms;
+    // Workers (clusters of cs CTAs: pairs, pairs of pairs, or single CTAs)
+    // the persistent grid holds at once.
+    const int cs = cg * mc;
+    int64_t slots = (cs == 4) ? max_quads : (cs == 2) ? max_pairs : num_sms;
     if (opts.max_ctas > 0)
-        slots = std::max<int64_t>(1, std::min<int64_t>(slots, opts.max_ctas / cg));
+        slots = std::max<int64_t>(1, std::min<int64_t>(slots, opts.max_ctas / cs));
     if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_CLC)
         return BWGEMM_ERR_INVALID_ARG;
     const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
@@ -112,7 +129,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     }
 
     int64_t s = 1, dp_tiles = tiles, sk_tiles = 0, workers = 0, ws = 0;
-    const int64_t slot_bytes = int64_t(cg) * kRowsPerCta * bn * 4;  // one piece's fp32 partial
+    const int64_t slot_bytes = int64_t(cs) * kRowsPerCta * bn * 4;  // one piece's fp32 partial
     if (stream_k) {
         dp_tiles = (tiles >= 2 * slots) ? (tiles / slots - 1) * slots : 0;
         sk_tiles = tiles - dp_tiles;
@@ -120,7 +137,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
         // at least 4 K blocks per worker; all workers when there are whole tiles too
         workers = dp_tiles > 0 ? slots : std::max<int64_t>(1, std::min<int64_t>(slots, iters / 4));
         ws = int64_t(kCounterRegionBytes) + workers * 2 * slot_bytes;
-        const int64_t counters = sk_tiles * cg * kEpiWarps * kCountersPerWarp * 4;
+        const int64_t counters = sk_tiles * cs * kEpiWarps * kCountersPerWarp * 4;
         if (counters > int64_t(kCounterRegionBytes) || uint64_t(ws) > workspace_bytes) {
             if (opts.schedule == BWGEMM_SCHEDULE_STREAM_K)
                 return BWGEMM_ERR_WORKSPACE;
@@ -145,7 +162,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
             s = std::max<int64_t>(s, 1);
         }
         if (s > 1) {
-            const int64_t counters = tiles * cg * kEpiWarps * kCountersPerWarp * 4;
+            const int64_t counters = tiles * cs * kEpiWarps * kCountersPerWarp * 4;
             ws = int64_t(kCounterRegionBytes) + tiles * s * slot_bytes;
             if (counters > int64_t(kCounterRegionBytes) || uint64_t(ws) > workspace_bytes) {
                 if (opts.split_k > 1)
@@ -180,7 +197,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.cfg.raster_group = int32_t(group);
     sel.cfg.num_tiles = int32_t(tiles);
     sel.cfg.num_units = int32_t(dp_tiles * s);
-    sel.cfg.grid = int32_t(workers * cg);
+    sel.cfg.grid = int32_t(workers * cs);
     sel.cfg.workspace_bytes = ws;
     sel.cfg.schedule = clc ? BWGEMM_SCHEDULE_CLC
                            : (stream_k ? BWGEMM_SCHEDULE_STREAM_K : BWGEMM_SCHEDULE_TILES);
@@ -189,6 +206,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int64_t M, int64_t N, 
     sel.cfg.workers = int32_t(workers);
     sel.cfg.split_scatter = scatter ? 1 : 0;
     sel.cfg.swap_ab = swap ? 1 : 0;
+    sel.cfg.multicast = mc;
     *out = sel;
     return BWGEMM_OK;
 }
@@ -275,7 +293,7 @@ bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t
         bwgemm_default_options(&o);
     const uint64_t ws = o.workspace_bytes ? o.workspace_bytes : (64ull << 20);
     Selection sel;
-    const bwgemm_status_t st = select_config(num_sms, max_pairs, M, N, K, o, ws, &sel);
+    const bwgemm_status_t st = select_config(num_sms, max_pairs, 0, M, N, K, o, ws, &sel);
     if (st == BWGEMM_OK)
         *out = sel.cfg;
     return st;

@@ -95,7 +95,11 @@ typedef struct {
                                  shared-memory loads: 0 = default (none), -1 = none     */
     int32_t swap_ab;          /* 0 = auto, 1 = never, 2 = always: compute C^T = B A^T so
                                  that B's rows fill the 128-row MMA side (small M)       */
-    int32_t reserved[3];      /* must be zero                                            */
+    int32_t multicast;        /* 0 = auto, 1 = off, 2 = on: clusters of two CTA pairs on
+                                 adjacent column blocks; each A tile is read from L2
+                                 once and multicast to both pairs (CTA-pair variant,
+                                 operands not swapped)                                   */
+    int32_t reserved[2];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -115,11 +119,14 @@ typedef struct {
     int32_t schedule;     /* BWGEMM_SCHEDULE_TILES, _STREAM_K or _CLC            */
     int32_t dp_tiles;     /* tiles computed whole (or as split_k slices)         */
     int32_t sk_tiles;     /* tiles whose K iterations are spread by stream-K     */
-    int32_t workers;      /* CTAs or CTA pairs of the persistent grid            */
+    int32_t workers;      /* clusters (CTAs, CTA pairs or pairs of pairs) of the
+                             persistent grid                                     */
     int32_t split_scatter; /* 1: the split_k slices of each tile run in one wave
                               and reduce-scatter their partials                  */
     int32_t swap_ab;      /* 1: operands swapped (tiles over C^T: tile_m along N,
                              tile_n along M)                                     */
+    int32_t multicast;    /* CTA pairs per cluster sharing each A tile (1 or 2);
+                             a tile then spans tile_n x multicast columns        */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */
@@ -191,7 +198,8 @@ bwgemm_status_t bwgemm_check_args(const void* A, const void* B, const void* C, i
 /*
  * Host-only: the configuration a plan with `opts` (NULL = defaults) would
  * pick for this shape on a GPU with `num_sms` SMs that can hold
- * `max_pairs` co-resident CTA pairs (0 = num_sms / 2).  No device access.
+ * `max_pairs` co-resident CTA pairs (0 = num_sms / 2) and max_pairs / 2
+ * co-resident clusters of two pairs (the multicast form).  No device access.
  */
 bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
                                      int64_t K, bwgemm_dtype_t dtype,

@@ -189,6 +189,31 @@ def test_select_cluster_launch_control():
         cfg(4096, 4096, 4096, schedule=4)
 
 
+def test_select_multicast_pairs_of_pairs():
+    # two CTA pairs per cluster on adjacent column blocks: a tile is 256 x 512
+    c = cfg(4096, 4096, 4096, sms=152, pairs=76, multicast=2, schedule=binding.SCHEDULE_TILES)
+    assert c["multicast"] == 2 and c["variant"] == 2 and c["tile_n"] == 256
+    assert c["num_tiles"] == 16 * 8 and c["workers"] == 38 and c["grid"] == 152
+    # an odd number of column blocks: the last group's second block is padding
+    c = cfg(1024, 768, 512, sms=152, pairs=76, multicast=2)
+    assert c["num_tiles"] == 4 * 2
+    c = cfg(4096, 4096, 4096, sms=152, pairs=76, multicast=2, schedule=binding.SCHEDULE_STREAM_K)
+    assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["grid"] == 152
+    assert c["dp_tiles"] + c["sk_tiles"] == 128 and c["dp_tiles"] % 38 == 0
+    c = cfg(4096, 4096, 4096, sms=152, pairs=76, multicast=2, schedule=binding.SCHEDULE_CLC)
+    assert c["grid"] == 4 * 128
+    c = cfg(4096, 4096, 4096, sms=152, pairs=76, multicast=2, tile_n=128, schedule=1)
+    assert c["num_tiles"] == 16 * 16 and c["tile_n"] == 128
+    assert cfg(4096, 4096, 4096, sms=152, pairs=76)["multicast"] == 1
+    assert cfg(4096, 4096, 4096, sms=152, pairs=76, multicast=1)["multicast"] == 1
+    with pytest.raises(binding.BwgemmError):
+        cfg(4096, 4096, 4096, multicast=2, variant=1)  # multicast joins CTA pairs
+    with pytest.raises(binding.BwgemmError):
+        cfg(32, 4096, 4096, multicast=2, swap_ab=2)
+    with pytest.raises(binding.BwgemmError):
+        cfg(4096, 4096, 4096, multicast=3)
+
+
 def test_select_tiles_schedule_splits_k():
     c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2

@@ -181,6 +181,66 @@ def test_cluster_launch_control_normal_inputs():
         run_full(p, A, B, "bf16")
 
 
+@pytest.mark.parametrize("opts", [dict(variant=2), dict(variant=1), dict(multicast=2),
+                                  dict(swap_ab=2), dict(variant=2, split_k=2),
+                                  dict(schedule=binding.SCHEDULE_STREAM_K)])
+@pytest.mark.parametrize("N", [1300, 1297])
+def test_columns_past_n_untouched(opts, N):
+    # N not a multiple of 8: the last 16-byte chunk of each row of C straddles
+    # the end of the row; the columns after N belong to the caller
+    M, K = 200, 320
+    A = make_matrix(M, K, "int2", seed=2900, device="cuda")
+    B = make_matrix(N, K, "int2", seed=2901, device="cuda")
+    C = torch.full((M, 1320), 7.0, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0, **opts) as p:
+        run_full(p, A, B, "bf16", exact=True, out=C[:, :N])
+    assert torch.all(C[:, N:] == 7.0)
+
+
+# ------------------------------------------------- A multicast across two pairs
+@pytest.mark.parametrize("M,N,K", [(512, 1024, 192), (300, 768, 200), (1000, 1300, 520),
+                                   (256, 256, 64)])
+@pytest.mark.parametrize("tile_n", [256, 128])
+def test_multicast_integers_exact(M, N, K, tile_n):
+    # ragged M / N / K; an odd count of column blocks leaves the second pair
+    # of the last group on padding columns (its boxes are never stored)
+    ldc = (N + 7) // 8 * 8
+    A = make_matrix(M, K, "int2", seed=2500 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=2600 + N, device="cuda")
+    C = torch.full((M, ldc), 7.0, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0, multicast=2, tile_n=tile_n, schedule=binding.SCHEDULE_TILES) as p:
+        for _ in range(2):
+            run_full(p, A, B, "bf16", exact=True, out=C[:, :N])
+        c = p.last_config()
+        assert c["multicast"] == 2 and c["grid"] % 4 == 0
+    assert torch.all(C[:, N:] == 7.0)
+
+
+@pytest.mark.parametrize("schedule,split_k", [(binding.SCHEDULE_STREAM_K, 0),
+                                              (binding.SCHEDULE_TILES, 3),
+                                              (binding.SCHEDULE_CLC, 0)])
+def test_multicast_schedules_exact(schedule, split_k):
+    A = make_matrix(1536, 1024, "int2", seed=2700, device="cuda")
+    B = make_matrix(2560, 1024, "int2", seed=2701, device="cuda")
+    with binding.Plan(0, multicast=2, schedule=schedule, split_k=split_k, max_ctas=40) as p:
+        for _ in range(2):
+            run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["multicast"] == 2 and c["schedule"] == schedule
+        if split_k:
+            assert c["split_k"] == split_k
+        if schedule == binding.SCHEDULE_STREAM_K:
+            assert c["sk_tiles"] > 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_multicast_normal_inputs(dtype):
+    A = make_matrix(2000, 1000, "normal", dtype, seed=2800, device="cuda")
+    B = make_matrix(3000, 1000, "weight", dtype, seed=2801, device="cuda")
+    with binding.Plan(0, multicast=2) as p:
+        run_full(p, A, B, dtype)
+
+
 def test_split_k_normal_inputs():
     A = make_matrix(200, 4096, "normal", seed=910, device="cuda")
     B = make_matrix(384, 4096, "weight", seed=911, device="cuda")

@@ -68,7 +68,8 @@ class PlanOptions(ctypes.Structure):
         ("prefetch", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("copy_kblocks", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 
@@ -92,6 +93,7 @@ class Config(ctypes.Structure):
         ("split_scatter", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
+        ("copy_kblocks", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -40,6 +40,7 @@ EncodeTiledFn encode_fn()
 struct TmapSlot {
     const void* ptr = nullptr;
     int64_t inner = 0, outer = 0, ld = 0;
+    int64_t chunks = 0;  // 3-D K-chunk views: number of whole 64-element chunks (0: 2-D map)
     int dtype = -1;
     uint32_t box_inner = 0, box_outer = 0;
     int swizzle = -1;
@@ -52,7 +53,7 @@ struct TmapSlot {
 bwgemm_status_t get_tmap(TmapSlot& s, const void* ptr, int dtype, int64_t inner, int64_t outer,
                          int64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
 {
-    if (s.valid && s.ptr == ptr && s.inner == inner && s.outer == outer && s.ld == ld &&
+    if (s.valid && s.chunks == 0 && s.ptr == ptr && s.inner == inner && s.outer == outer && s.ld == ld &&
         s.dtype == dtype && s.box_inner == box_inner && s.box_outer == box_outer &&
         s.swizzle == int(swz))
         return BWGEMM_OK;
@@ -76,10 +77,51 @@ bwgemm_status_t get_tmap(TmapSlot& s, const void* ptr, int dtype, int64_t inner,
     s.inner = inner;
     s.outer = outer;
     s.ld = ld;
+    s.chunks = 0;
     s.dtype = dtype;
     s.box_inner = box_inner;
     s.box_outer = box_outer;
     s.swizzle = int(swz);
+    s.valid = true;
+    return BWGEMM_OK;
+}
+
+// Build (or reuse) a 3-D view of a K-major operand for copies of two K blocks
+// at once: dimension 0 = the 64 elements of one K chunk, 1 = rows (ld apart),
+// 2 = whole K chunks (128 bytes apart).  A box {64, box_rows, 2} lands as two
+// consecutive 128-byte-swizzled [box_rows x 64] blocks, i.e. two adjacent ring
+// stages.  Only whole chunks are described, so no copy reads past K.
+bwgemm_status_t get_tmap3(TmapSlot& s, const void* ptr, int dtype, int64_t chunks, int64_t rows,
+                          int64_t ld, uint32_t box_rows)
+{
+    if (s.valid && s.chunks == chunks && s.ptr == ptr && s.outer == rows && s.ld == ld &&
+        s.dtype == dtype && s.box_outer == box_rows)
+        return BWGEMM_OK;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return BWGEMM_ERR_NO_DEVICE;
+    const cuuint64_t dims[3] = {cuuint64_t(kTileK), cuuint64_t(rows), cuuint64_t(chunks)};
+    const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, cuuint64_t(kTileK) * 2};
+    const cuuint32_t box[3] = {uint32_t(kTileK), box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    s.valid = false;
+    const CUresult r = enc(&s.map,
+                           dtype == BWGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           3, const_cast<void*>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return BWGEMM_ERR_CUDA;
+    s.ptr = ptr;
+    s.inner = kTileK;
+    s.outer = rows;
+    s.ld = ld;
+    s.chunks = chunks;
+    s.dtype = dtype;
+    s.box_inner = kTileK;
+    s.box_outer = box_rows;
+    s.swizzle = int(CU_TENSOR_MAP_SWIZZLE_128B);
     s.valid = true;
     return BWGEMM_OK;
 }
@@ -111,7 +153,7 @@ struct bwgemm_plan_s {
     uint32_t* d_status = nullptr;
     uint8_t* d_workspace = nullptr;
     uint64_t workspace_bytes = 0;
-    TmapSlot tmaps[3];
+    TmapSlot tmaps[5];  // A, B, C, and the 3-D two-K-block views of A and B
     bwgemm_config_t last;
     uint64_t launches = 0;
     uint32_t last_status_bits = 0;
@@ -164,7 +206,20 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
                        CU_TENSOR_MAP_SWIZZLE_64B)) != BWGEMM_OK)
         return st;
 
+    // copies of two K blocks at once need at least two whole K chunks; with
+    // A multicast only B is copied that way
+    const int64_t chunks = K / kTileK;
+    const bool pair_copies = sel.cfg.copy_kblocks == 2 && chunks >= 2;
+    if (pair_copies) {
+        if (v.mc == 1 &&
+            (st = get_tmap3(plan->tmaps[3], opA, dtype, chunks, rowsA, ldA, uint32_t(kRowsPerCta))) != BWGEMM_OK)
+            return st;
+        if ((st = get_tmap3(plan->tmaps[4], opB, dtype, chunks, rowsB, ldB, b_rows)) != BWGEMM_OK)
+            return st;
+    }
+
     GemmParams p = make_params(sel, M, N, K, dtype);
+    p.k_chunks = pair_copies ? int32_t(chunks) : 0;
     p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
     p.status = plan->d_status;
     p.c = static_cast<uint16_t*>(C);
@@ -183,8 +238,10 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
         p.trace = plan->d_trace;
     }
 
+    const CUtensorMap& a2 = (pair_copies && v.mc == 1) ? plan->tmaps[3].map : plan->tmaps[0].map;
+    const CUtensorMap& b2 = pair_copies ? plan->tmaps[4].map : plan->tmaps[1].map;
     const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
-                                           plan->tmaps[2].map, p, sel.cfg.grid, stream,
+                                           plan->tmaps[2].map, a2, b2, p, sel.cfg.grid, stream,
                                            plan->opts.pdl_off == 0);
     if (err != cudaSuccess)
         return BWGEMM_ERR_CUDA;

@@ -486,7 +486,8 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
 template <int CG, int BN, int STAGES, bool TR, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
+                const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_a2,
+                const __grid_constant__ CUtensorMap tmap_b2, const GemmParams p)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
     static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
@@ -540,6 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_c);
+        if (p.k_chunks > 1) {
+            ptx::prefetch_tensormap(&tmap_a2);
+            ptx::prefetch_tensormap(&tmap_b2);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
@@ -564,26 +569,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            bool first_unit = true;
-            int requested = 0;
-            Sched iter;
-            iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
-            WorkUnit w;
-            while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusProducerTimeout)) {
-                if (p.clc) {
-                    // ask for the tile after this one now, a whole tile ahead of need
-                    const int rq = requested++;
-                    const int slot = rq % kClcSlots;
-                    if (rank == 0 &&
-                        !wait_phase(bar_clc_empty + 8 * slot, (uint32_t(rq / kClcSlots) & 1u) ^ 1u, p,
-                                    abort_flag, kStatusProducerTimeout)) {
-                        ok = false;
+        // The whole warp walks the unit and K-block sequence, so the loop state
+        // is warp-uniform, and lane 0 issues the copies and barrier updates.
+        // (Run by lane 0 alone, every TMA instruction first moved its
+        // per-thread operands into uniform registers; that bookkeeping cost
+        // more than a K block's MMAs and left the tensor pipe waiting.)
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool first_unit = true;
+        int requested = 0;
+        Sched iter;
+        iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
+        WorkUnit w;
+        // both CTAs' bytes of a pair are counted on the pair leader's barrier
+        const uint32_t leader_full = (CG == 2) ? ptx::map_to_cta(bar_full, leader) : bar_full;
+        while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusProducerTimeout)) {
+            if (p.clc) {
+                // ask for the tile after this one now, a whole tile ahead of need
+                const int rq = requested++;
+                const int slot = rq % kClcSlots;
+                if (rank == 0) {
+                    ok = __all_sync(0xffffffffu,
+                                    wait_phase(bar_clc_empty + 8 * slot, (uint32_t(rq / kClcSlots) & 1u) ^ 1u,
+                                               p, abort_flag, kStatusProducerTimeout));
+                    if (!ok)
                         break;
-                    }
+                }
+                if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(bar_clc_full + 8 * slot, 16);
                     if (rank == 0) {
                         if constexpr (CS == 1)
@@ -592,68 +605,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::clc_try_cancel_all(clc_resp + 16 * slot, bar_clc_full + 8 * slot);
                     }
                 }
-                const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
-                const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
-                // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
-                // ring only has to cover L2 latency, not DRAM latency
-                const int pf = p.prefetch;
+                __syncwarp();
+            }
+            const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
+            const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
+            // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
+            // ring only has to cover L2 latency, not DRAM latency
+            const int pf = p.prefetch;
+            if (lane == 0) {
                 for (int kb = w.kb0; kb < min(w.kb1, w.kb0 + pf); ++kb) {
                     ptx::tma_prefetch_2d(&tmap_a, kb * kTileK, a_row);
                     ptx::tma_prefetch_2d(&tmap_b, kb * kTileK, b_row);
                 }
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (pf > 0 && kb + pf < w.kb1) {
-                        ptx::tma_prefetch_2d(&tmap_a, (kb + pf) * kTileK, a_row);
-                        ptx::tma_prefetch_2d(&tmap_b, (kb + pf) * kTileK, b_row);
-                    }
-                    if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, p, abort_flag,
-                                    kStatusProducerTimeout)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 && first_unit &&
-                                       kb - w.kb0 == p.stall_kblock;
-                    if (!stall) {
-                        if (first_unit && kb == w.kb0)
-                            trace_mark(p, kTraceFirstLoad);
-                        const uint32_t fb = bar_full + 8 * stage;
-                        const uint32_t dA = sA + stage * Cfg::kABytes;
-                        const uint32_t dB = sB + stage * Cfg::kBBytes;
-                        if constexpr (CG == 1) {
-                            ptx::mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                            ptx::tma_load_2d(dA, &tmap_a, fb, kb * kTileK, a_row);
-                            ptx::tma_load_2d(dB, &tmap_b, fb, kb * kTileK, b_row);
-                        } else {
-                            // both CTAs' bytes are counted on the pair leader's barrier
-                            const uint32_t leader_fb = ptx::map_to_cta(fb, leader);
-                            if (prank == 0)
-                                ptx::mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-                            if constexpr (MC == 1) {
-                                ptx::tma_load_2d_pair(dA, &tmap_a, leader_fb, kb * kTileK, a_row);
-                            } else {
-                                // rows [pair * 128 / MC, +128 / MC) of this CTA's 128, into
-                                // the same place in every CTA of the cluster with this prank
-                                constexpr int kPart = kRowsPerCta / MC;
-                                uint16_t mask = 0;
-#pragma unroll
-                                for (int i = 0; i < MC; ++i)
-                                    mask |= uint16_t(1u << (int(prank) + CG * i));
-                                ptx::tma_load_2d_pair_multicast(
-                                    dA + uint32_t(pair) * uint32_t(kPart * kTileK * 2), &tmap_a, leader_fb,
-                                    kb * kTileK, a_row + int(pair) * kPart, mask);
-                            }
-                            ptx::tma_load_2d_pair(dB, &tmap_b, leader_fb, kb * kTileK, b_row);
-                        }
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+            }
+            for (int kb = w.kb0; kb < w.kb1;) {
+                // Two K blocks in one copy per operand (3-D maps) when both are
+                // whole 64-element chunks and the next ring stage follows this
+                // one: a TMA copy costs about as much as 140 ns of its unit's
+                // time whatever its size, so one copy per K block of 16 KiB
+                // cannot keep up with the MMAs.  Both stages' bytes complete on
+                // this stage's full barrier; the next stage's barrier only gets
+                // an arrival (the MMA warp always consumes this stage first).
+                const bool dbl = (stage % 2 == 0) && (stage + 1 < STAGES) && (kb + 1 < w.kb1) &&
+                                 (kb + 1 < p.k_chunks);
+                const int nkb = dbl ? 2 : 1;
+                if (pf > 0 && lane == 0) {
+                    for (int j = kb + pf; j < min(kb + pf + nkb, w.kb1); ++j) {
+                        ptx::tma_prefetch_2d(&tmap_a, j * kTileK, a_row);
+                        ptx::tma_prefetch_2d(&tmap_b, j * kTileK, b_row);
                     }
                 }
-                first_unit = false;
+                ok = __all_sync(0xffffffffu, wait_phase(bar_empty + 8 * stage, phase ^ 1u, p, abort_flag,
+                                                        kStatusProducerTimeout));
+                if (ok && dbl)
+                    ok = __all_sync(0xffffffffu, wait_phase(bar_empty + 8 * (stage + 1), phase ^ 1u, p,
+                                                            abort_flag, kStatusProducerTimeout));
+                if (!ok)
+                    break;
+                const int rel = kb - w.kb0;
+                const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 && first_unit &&
+                                   p.stall_kblock >= rel && p.stall_kblock < rel + nkb;
+                if (!stall && lane == 0) {
+                    if (first_unit && kb == w.kb0)
+                        trace_mark(p, kTraceFirstLoad);
+                    const uint32_t fb = bar_full + 8 * stage;
+                    const uint32_t dA = sA + stage * Cfg::kABytes;
+                    const uint32_t dB = sB + stage * Cfg::kBBytes;
+                    const uint32_t tx = Cfg::kTxBytes * uint32_t(nkb);
+                    if constexpr (CG == 1) {
+                        ptx::mbar_arrive_expect_tx(fb, tx);
+                        if (dbl) {
+                            ptx::mbar_arrive(fb + 8);
+                            ptx::tma_load_3d(dA, &tmap_a2, fb, 0, a_row, kb);
+                            ptx::tma_load_3d(dB, &tmap_b2, fb, 0, b_row, kb);
+                        } else {
+                            ptx::tma_load_2d(dA, &tmap_a, fb, kb * kTileK, a_row);
+                            ptx::tma_load_2d(dB, &tmap_b, fb, kb * kTileK, b_row);
+                        }
+                    } else {
+                        const uint32_t lfb = leader_full + 8 * stage;
+                        if (prank == 0) {
+                            ptx::mbar_arrive_expect_tx(fb, tx);
+                            if (dbl)
+                                ptx::mbar_arrive(fb + 8);
+                        }
+                        if constexpr (MC == 1) {
+                            if (dbl)
+                                ptx::tma_load_3d_pair(dA, &tmap_a2, lfb, 0, a_row, kb);
+                            else
+                                ptx::tma_load_2d_pair(dA, &tmap_a, lfb, kb * kTileK, a_row);
+                        } else {
+                            // rows [pair * 128 / MC, +128 / MC) of this CTA's 128, into
+                            // the same place in every CTA of the cluster with this
+                            // prank (one copy per K block: the part is not a whole
+                            // ring stage, so two of them are not contiguous)
+                            constexpr int kPart = kRowsPerCta / MC;
+                            uint16_t mask = 0;
+#pragma unroll
+                            for (int i = 0; i < MC; ++i)
+                                mask |= uint16_t(1u << (int(prank) + CG * i));
+                            for (int j = 0; j < nkb; ++j)
+                                ptx::tma_load_2d_pair_multicast(
+                                    dA + uint32_t(j * Cfg::kABytes) + uint32_t(pair) * uint32_t(kPart * kTileK * 2),
+                                    &tmap_a, lfb, (kb + j) * kTileK, a_row + int(pair) * kPart, mask);
+                        }
+                        if (dbl)
+                            ptx::tma_load_3d_pair(dB, &tmap_b2, lfb, 0, b_row, kb);
+                        else
+                            ptx::tma_load_2d_pair(dB, &tmap_b, lfb, kb * kTileK, b_row);
+                    }
+                }
+                __syncwarp();
+                kb += nkb;
+                stage += nkb;
+                if (stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            trace_mark(p, kTraceLastLoad);
+            first_unit = false;
         }
+        if (lane == 0)
+            trace_mark(p, kTraceLastLoad);
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0 && prank == 0) {

@@ -37,11 +37,13 @@ int find_variant(int cg, int bn, bool trans, int mc = 1);
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);
 
-// Launch variant `idx` with `grid` CTAs (a multiple of its CTA group); with
-// `pdl`, as a programmatic dependent launch (its prologue may overlap the
-// previous kernel on the stream).
+// Launch variant `idx` with `grid` CTAs (a multiple of its cluster size);
+// with `pdl`, as a programmatic dependent launch (its prologue may overlap the
+// previous kernel on the stream).  a2 / b2: 3-D views of the operands that
+// copy two K blocks at once (used only when p.k_chunks > 1).
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+                           const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p, int grid,
+                           cudaStream_t stream, bool pdl);
 
 // Co-resident clusters (of cg * mc CTAs; single CTAs for cg * mc == 1) of
 // variant `idx` on the current device.

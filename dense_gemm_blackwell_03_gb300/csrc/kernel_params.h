@@ -72,6 +72,8 @@ struct GemmParams {
     uint64_t* trace;        // optional timeline: kTraceSlots %globaltimer stamps per CTA (null: off)
     uint16_t* c;            // C itself, for the boxes a TMA store cannot clip exactly
     int64_t ldc;            // elements between rows of C
+    int32_t k_chunks;       // whole 64-element K chunks the 3-D operand maps cover
+                            // (floor(K / 64)); 0: every copy is one K block
 };
 
 // Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).

@@ -183,7 +183,8 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     p.ldc = ldc;
     p.tile_sems = ctr;
     p.partials = reinterpret_cast<float*>(partials);
-    return launch_variant(sel.variant_idx, ta, tb, tc, p, sel.cfg.grid, s, false) == cudaSuccess
+    p.k_chunks = 0;  // one copy per K block: the 3-D operand views are not built here
+    return launch_variant(sel.variant_idx, ta, tb, tc, ta, tb, p, sel.cfg.grid, s, false) == cudaSuccess
                ? BWGEMM_OK
                : BWGEMM_ERR_CUDA;
 }

@@ -79,7 +79,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     if (idx < 0)
         return BWGEMM_ERR_UNSUPPORTED;
     if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0 || opts.prefetch < -1 ||
-        opts.prefetch > 64)
+        opts.prefetch > 64 || opts.copy_kblocks < 0 || opts.copy_kblocks > 2)
         return BWGEMM_ERR_INVALID_ARG;
 
     const int tile_m = kRowsPerCta * cg;
@@ -207,6 +207,15 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.split_scatter = scatter ? 1 : 0;
     sel.cfg.swap_ab = swap ? 1 : 0;
     sel.cfg.multicast = mc;
+    // K blocks per operand copy.  Two (3-D copies) when the kernel is compute
+    // bound: one TMA copy occupies its unit for ~140 ns whatever its size, and
+    // two 16 KiB copies per K block take longer than the K block's MMAs.  In
+    // a memory-bound decode shape (a side of at most 256 rows) the coarser
+    // stages cost more than the copies they save, so one.
+    if (opts.copy_kblocks == 0)
+        sel.cfg.copy_kblocks = (std::min(Mk, Nk) > 256 && num_kb >= 2) ? 2 : 1;
+    else
+        sel.cfg.copy_kblocks = opts.copy_kblocks;
     *out = sel;
     return BWGEMM_OK;
 }

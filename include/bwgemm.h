@@ -99,7 +99,10 @@ typedef struct {
                                  adjacent column blocks; each A tile is read from L2
                                  once and multicast to both pairs (CTA-pair variant,
                                  operands not swapped)                                   */
-    int32_t reserved[2];      /* must be zero                                            */
+    int32_t copy_kblocks;     /* K blocks per TMA operand copy: 0 = auto (two for
+                                 compute-bound shapes), 1 = one, 2 = two (where K holds
+                                 at least two whole 64-element chunks)                   */
+    int32_t reserved[1];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -127,6 +130,8 @@ typedef struct {
                              tile_n along M)                                     */
     int32_t multicast;    /* CTA pairs per cluster sharing each A tile (1 or 2);
                              a tile then spans tile_n x multicast columns        */
+    int32_t copy_kblocks; /* K blocks per TMA operand copy (1 or 2; 2 applies
+                             where K holds at least two whole 64-element chunks) */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

@@ -212,6 +212,19 @@ def test_select_multicast_pairs_of_pairs():
         cfg(32, 4096, 4096, multicast=2, swap_ab=2)
     with pytest.raises(binding.BwgemmError):
         cfg(4096, 4096, 4096, multicast=3)
+    with pytest.raises(binding.BwgemmError):
+        cfg(4096, 4096, 4096, copy_kblocks=3)
+    assert cfg(4096, 4096, 4096, copy_kblocks=1)["copy_kblocks"] == 1
+
+
+def test_select_kblocks_per_copy():
+    # two K blocks per operand copy for compute-bound shapes, one for decode
+    assert cfg(4096, 4096, 4096, sms=152, pairs=76)["copy_kblocks"] == 2
+    assert cfg(512, 8192, 5376, sms=152, pairs=76)["copy_kblocks"] == 2
+    assert cfg(256, 28672, 8192, sms=152, pairs=76)["copy_kblocks"] == 1
+    assert cfg(32, 8192, 8192, sms=152, pairs=76)["copy_kblocks"] == 1  # swapped: N' = 32
+    assert cfg(256, 28672, 8192, sms=152, pairs=76, copy_kblocks=2)["copy_kblocks"] == 2
+    assert cfg(4096, 4096, 64, sms=152, pairs=76)["copy_kblocks"] == 1  # one K block
 
 
 def test_select_tiles_schedule_splits_k():

@@ -197,6 +197,34 @@ def test_columns_past_n_untouched(opts, N):
     assert torch.all(C[:, N:] == 7.0)
 
 
+# ------------------------------------- two K blocks per TMA copy (3-D operand views)
+@pytest.mark.parametrize("K", [64, 128, 192, 200, 1000, 1088])
+@pytest.mark.parametrize("opts", [dict(variant=2), dict(variant=1), dict(variant=1, tile_n=128),
+                                  dict(variant=2, tile_n=128), dict(multicast=2),
+                                  dict(schedule=binding.SCHEDULE_STREAM_K, max_ctas=24),
+                                  dict(variant=2, split_k=3, schedule=binding.SCHEDULE_TILES)])
+def test_paired_kblock_copies_exact(opts, K):
+    # one chunk (no pairs), pairs only, pairs + a single, + a ragged tail;
+    # stream-K and split-K units start at odd K blocks and odd ring stages
+    A = make_matrix(520, K, "int2", seed=3000 + K, device="cuda")
+    B = make_matrix(696, K, "int2", seed=3100 + K, device="cuda")
+    outs = []
+    for copy_kblocks in (1, 2):
+        with binding.Plan(0, copy_kblocks=copy_kblocks, **opts) as p:
+            _, C = run_full(p, A, B, "bf16", exact=True)
+            outs.append(C.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("swap", [2])
+def test_paired_kblock_copies_swapped(swap):
+    A = make_matrix(40, 1000, "int2", seed=3200, device="cuda")
+    B = make_matrix(3000, 1000, "int2", seed=3201, device="cuda")
+    with binding.Plan(0, swap_ab=swap, copy_kblocks=2) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        assert p.last_config()["swap_ab"] == 1 and p.last_config()["copy_kblocks"] == 2
+
+
 # ------------------------------------------------- A multicast across two pairs
 @pytest.mark.parametrize("M,N,K", [(512, 1024, 192), (300, 768, 200), (1000, 1300, 520),
                                    (256, 256, 64)])

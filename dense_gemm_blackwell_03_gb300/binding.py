@@ -94,6 +94,8 @@ class Config(ctypes.Structure):
         ("swap_ab", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
         ("copy_kblocks", ctypes.c_int32),
+        ("prefetch_kblocks", ctypes.c_int32),
+        ("prefetch_b", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -206,20 +206,22 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
                        CU_TENSOR_MAP_SWIZZLE_64B)) != BWGEMM_OK)
         return st;
 
-    // copies of two K blocks at once need at least two whole K chunks; with
-    // A multicast only B is copied that way
+    GemmParams p = make_params(sel, M, N, K, dtype);
+    // 3-D views (two K blocks per copy or prefetch) need at least two whole K
+    // chunks; with A multicast each CTA copies part of a stage of A, which a
+    // 3-D view of whole stages does not describe
     const int64_t chunks = K / kTileK;
     const bool pair_copies = sel.cfg.copy_kblocks == 2 && chunks >= 2;
-    if (pair_copies) {
-        if (v.mc == 1 &&
-            (st = get_tmap3(plan->tmaps[3], opA, dtype, chunks, rowsA, ldA, uint32_t(kRowsPerCta))) != BWGEMM_OK)
-            return st;
-        if ((st = get_tmap3(plan->tmaps[4], opB, dtype, chunks, rowsB, ldB, b_rows)) != BWGEMM_OK)
-            return st;
-    }
-
-    GemmParams p = make_params(sel, M, N, K, dtype);
-    p.k_chunks = pair_copies ? int32_t(chunks) : 0;
+    const bool view_a = chunks >= 2 && v.mc == 1 && (pair_copies || (p.prefetch > 0 && !p.prefetch_b));
+    const bool view_b = chunks >= 2 && (pair_copies || (p.prefetch > 0 && p.prefetch_b));
+    if (view_a &&
+        (st = get_tmap3(plan->tmaps[3], opA, dtype, chunks, rowsA, ldA, uint32_t(kRowsPerCta))) != BWGEMM_OK)
+        return st;
+    if (view_b && (st = get_tmap3(plan->tmaps[4], opB, dtype, chunks, rowsB, ldB, b_rows)) != BWGEMM_OK)
+        return st;
+    p.k_chunks_a = view_a ? int32_t(chunks) : 0;
+    p.k_chunks_b = view_b ? int32_t(chunks) : 0;
+    p.pair_copies = pair_copies ? 1 : 0;
     p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
     p.status = plan->d_status;
     p.c = static_cast<uint16_t*>(C);
@@ -227,8 +229,6 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     p.tile_sems = reinterpret_cast<uint32_t*>(plan->d_workspace);
     p.partials = reinterpret_cast<float*>(plan->d_workspace + kCounterRegionBytes);
     p.stall_kblock = plan->opts.stall_kblock;
-    if (plan->opts.prefetch != 0)
-        p.prefetch = plan->opts.prefetch < 0 ? 0 : plan->opts.prefetch;
     if (plan->d_trace) {
         if (sel.cfg.grid > plan->trace_ctas)
             return BWGEMM_ERR_UNSUPPORTED;
@@ -238,8 +238,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
         p.trace = plan->d_trace;
     }
 
-    const CUtensorMap& a2 = (pair_copies && v.mc == 1) ? plan->tmaps[3].map : plan->tmaps[0].map;
-    const CUtensorMap& b2 = pair_copies ? plan->tmaps[4].map : plan->tmaps[1].map;
+    const CUtensorMap& a2 = view_a ? plan->tmaps[3].map : plan->tmaps[0].map;
+    const CUtensorMap& b2 = view_b ? plan->tmaps[4].map : plan->tmaps[1].map;
     const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
                                            plan->tmaps[2].map, a2, b2, p, sel.cfg.grid, stream,
                                            plan->opts.pdl_off == 0);

@@ -541,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_c);
-        if (p.k_chunks > 1) {
+        if (p.k_chunks_a > 1)
             ptx::prefetch_tensormap(&tmap_a2);
+        if (p.k_chunks_b > 1)
             ptx::prefetch_tensormap(&tmap_b2);
-        }
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
@@ -609,15 +609,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
             const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
-            // L2 prefetch runs `prefetch` K blocks ahead of the loads, so the
-            // ring only has to cover L2 latency, not DRAM latency
+            // L2 prefetch of the streamed operand (the one read from DRAM, not
+            // shared by the tiles running at the same time) `prefetch` K
+            // blocks ahead of the loads: the DRAM reads in flight are then not
+            // bounded by the ring, and the ring's loads hit L2.  Two K blocks
+            // per prefetch where the 3-D maps describe them (each TMA
+            // instruction costs its unit the same time whatever its size).
             const int pf = p.prefetch;
-            if (lane == 0) {
-                for (int kb = w.kb0; kb < min(w.kb1, w.kb0 + pf); ++kb) {
-                    ptx::tma_prefetch_2d(&tmap_a, kb * kTileK, a_row);
-                    ptx::tma_prefetch_2d(&tmap_b, kb * kTileK, b_row);
+            const CUtensorMap* pf_map2 = p.prefetch_b ? &tmap_b2 : &tmap_a2;
+            const CUtensorMap* pf_map = p.prefetch_b ? &tmap_b : &tmap_a;
+            const int pf_row = p.prefetch_b ? b_row : a_row;
+            const int pf_chunks = p.prefetch_b ? p.k_chunks_b : p.k_chunks_a;
+            int pf_next = w.kb0;  // first K block not yet prefetched
+            auto prefetch_to = [&](int end) {
+                end = min(end, w.kb1);
+                while (pf_next < end) {
+                    if (pf_next + 1 < end && pf_next + 1 < pf_chunks) {
+                        ptx::tma_prefetch_3d(pf_map2, 0, pf_row, pf_next);
+                        pf_next += 2;
+                    } else {
+                        ptx::tma_prefetch_2d(pf_map, pf_next * kTileK, pf_row);
+                        pf_next += 1;
+                    }
                 }
-            }
+            };
+            if (pf > 0 && lane == 0)
+                prefetch_to(w.kb0 + pf);
             for (int kb = w.kb0; kb < w.kb1;) {
                 // Two K blocks in one copy per operand (3-D maps) when both are
                 // whole 64-element chunks and the next ring stage follows this
@@ -627,14 +644,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this stage's full barrier; the next stage's barrier only gets
                 // an arrival (the MMA warp always consumes this stage first).
                 const bool dbl = (stage % 2 == 0) && (stage + 1 < STAGES) && (kb + 1 < w.kb1) &&
-                                 (kb + 1 < p.k_chunks);
+                                 p.pair_copies && (kb + 1 < p.k_chunks_b) &&
+                                 (MC > 1 || kb + 1 < p.k_chunks_a);
                 const int nkb = dbl ? 2 : 1;
-                if (pf > 0 && lane == 0) {
-                    for (int j = kb + pf; j < min(kb + pf + nkb, w.kb1); ++j) {
-                        ptx::tma_prefetch_2d(&tmap_a, j * kTileK, a_row);
-                        ptx::tma_prefetch_2d(&tmap_b, j * kTileK, b_row);
-                    }
-                }
+                if (pf > 0 && lane == 0)
+                    prefetch_to(kb + nkb + pf);
                 ok = __all_sync(0xffffffffu, wait_phase(bar_empty + 8 * stage, phase ^ 1u, p, abort_flag,
                                                         kStatusProducerTimeout));
                 if (ok && dbl)

@@ -66,14 +66,17 @@ struct GemmParams {
     uint32_t* tile_sems;    // per (tile, cta, warp) arrival counters, zero between calls
     int32_t stall_kblock;   // test hook: producer never fills this k-block of its first unit (< 0: off)
     int32_t split_scatter;  // split-K in one wave: the slices of a tile reduce-scatter (see epilogue)
-    int32_t prefetch;       // K blocks the producer prefetches into L2 ahead of its loads (0: off)
+    int32_t prefetch;       // K blocks of the streamed operand the producer prefetches
+                            // into L2 ahead of its loads (0: off)
+    int32_t prefetch_b;     // the streamed operand: 1 = B, 0 = A
     int32_t clc;            // 1: one cluster per tile, running clusters take over pending ones
                             //    through cluster launch control (whole tiles only)
     uint64_t* trace;        // optional timeline: kTraceSlots %globaltimer stamps per CTA (null: off)
     uint16_t* c;            // C itself, for the boxes a TMA store cannot clip exactly
     int64_t ldc;            // elements between rows of C
-    int32_t k_chunks;       // whole 64-element K chunks the 3-D operand maps cover
-                            // (floor(K / 64)); 0: every copy is one K block
+    int32_t k_chunks_a;     // whole 64-element K chunks the 3-D view of A covers
+    int32_t k_chunks_b;     // (floor(K / 64)) and of B; 0: that view was not built
+    int32_t pair_copies;    // 1: load two K blocks per copy where the 3-D views allow
 };
 
 // Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).

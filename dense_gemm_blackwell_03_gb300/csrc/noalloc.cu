@@ -183,7 +183,10 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     p.ldc = ldc;
     p.tile_sems = ctr;
     p.partials = reinterpret_cast<float*>(partials);
-    p.k_chunks = 0;  // one copy per K block: the 3-D operand views are not built here
+    // one copy per K block and no prefetch: the 3-D operand views are not built here
+    p.k_chunks_a = p.k_chunks_b = 0;
+    p.pair_copies = 0;
+    p.prefetch = 0;
     return launch_variant(sel.variant_idx, ta, tb, tc, ta, tb, p, sel.cfg.grid, s, false) == cudaSuccess
                ? BWGEMM_OK
                : BWGEMM_ERR_CUDA;

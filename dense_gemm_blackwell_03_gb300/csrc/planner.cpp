@@ -13,6 +13,7 @@ namespace {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -216,6 +217,12 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         sel.cfg.copy_kblocks = (std::min(Mk, Nk) > 256 && num_kb >= 2) ? 2 : 1;
     else
         sel.cfg.copy_kblocks = opts.copy_kblocks;
+    // L2 prefetch of the streamed operand (the one with more rows: read from
+    // DRAM once, while the other stays in L2 for every tile): off unless
+    // asked for.  Measured on the decode and tail shapes at distances 4 to 32
+    // K blocks (one or two K blocks per prefetch) it was slower every time.
+    sel.cfg.prefetch_kblocks = opts.prefetch > 0 ? opts.prefetch : 0;
+    sel.cfg.prefetch_b = (Nk >= Mk) ? 1 : 0;
     *out = sel;
     return BWGEMM_OK;
 }
@@ -242,7 +249,8 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
     p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
     p.stall_kblock = -1;
     p.split_scatter = sel.cfg.split_scatter;
-    p.prefetch = 0;  // L2 prefetch ahead of the loads measured slower on every shape
+    p.prefetch = sel.cfg.prefetch_kblocks;
+    p.prefetch_b = sel.cfg.prefetch_b;
     p.clc = sel.cfg.schedule == BWGEMM_SCHEDULE_CLC ? 1 : 0;
     return p;
 }

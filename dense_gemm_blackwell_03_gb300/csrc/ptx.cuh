@@ -222,6 +222,15 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t 
                  : "memory");
 }
 
+// Prefetch one 3-D box (two K chunks of the 3-D operand views) into L2.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // 2-D tiled store shared -> global (out-of-range rows/columns are clipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1)

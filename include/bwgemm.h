@@ -91,8 +91,10 @@ typedef struct {
     int32_t pdl_off;          /* nonzero: launch without programmatic dependent launch  */
     int32_t trace;            /* nonzero: record a per-CTA timeline of every launch
                                  (read back with bwgemm_plan_read_trace)                */
-    int32_t prefetch;         /* K blocks of A and B prefetched into L2 ahead of the
-                                 shared-memory loads: 0 = default (none), -1 = none     */
+    int32_t prefetch;         /* K blocks of the streamed operand (the one with more
+                                 rows) prefetched into L2 ahead of the shared-memory
+                                 loads: 0 or -1 = none (measured slower on every shape),
+                                 n = n K blocks ahead                                    */
     int32_t swap_ab;          /* 0 = auto, 1 = never, 2 = always: compute C^T = B A^T so
                                  that B's rows fill the 128-row MMA side (small M)       */
     int32_t multicast;        /* 0 = auto, 1 = off, 2 = on: clusters of two CTA pairs on
@@ -132,6 +134,8 @@ typedef struct {
                              a tile then spans tile_n x multicast columns        */
     int32_t copy_kblocks; /* K blocks per TMA operand copy (1 or 2; 2 applies
                              where K holds at least two whole 64-element chunks) */
+    int32_t prefetch_kblocks; /* L2 prefetch distance of the streamed operand (0: off) */
+    int32_t prefetch_b;   /* the streamed operand: 1 = B (the kernel's), 0 = A   */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

@@ -217,6 +217,18 @@ def test_select_multicast_pairs_of_pairs():
     assert cfg(4096, 4096, 4096, copy_kblocks=1)["copy_kblocks"] == 1
 
 
+def test_select_prefetch():
+    c = cfg(256, 8192, 8192, sms=152, pairs=76)
+    assert c["prefetch_kblocks"] == 0 and c["prefetch_b"] == 1  # off unless asked for
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, prefetch=8)
+    assert c["prefetch_kblocks"] == 8 and c["prefetch_b"] == 1
+    c = cfg(16, 8192, 8192, sms=152, pairs=76, prefetch=8)
+    assert c["swap_ab"] == 1 and c["prefetch_b"] == 0  # swapped: the weights are the kernel's A
+    assert cfg(256, 8192, 8192, prefetch=-1)["prefetch_kblocks"] == 0
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 8192, 8192, prefetch=65)
+
+
 def test_select_kblocks_per_copy():
     # two K blocks per operand copy for compute-bound shapes, one for decode
     assert cfg(4096, 4096, 4096, sms=152, pairs=76)["copy_kblocks"] == 2

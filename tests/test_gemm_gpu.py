@@ -216,6 +216,19 @@ def test_paired_kblock_copies_exact(opts, K):
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("prefetch,opts", [(4, dict()), (3, dict(copy_kblocks=2)), (8, dict(swap_ab=2)),
+                                           (6, dict(multicast=2)), (5, dict(schedule=binding.SCHEDULE_STREAM_K))])
+def test_l2_prefetch_exact(prefetch, opts):
+    # the prefetch stream of the operand with more rows (2-D or 3-D boxes)
+    # changes no result
+    A = make_matrix(264, 1000, "int2", seed=3300, device="cuda")
+    B = make_matrix(2000, 1000, "int2", seed=3301, device="cuda")
+    with binding.Plan(0, prefetch=prefetch, **opts) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["prefetch_kblocks"] == prefetch and c["prefetch_b"] == (0 if c["swap_ab"] else 1)
+
+
 @pytest.mark.parametrize("swap", [2])
 def test_paired_kblock_copies_swapped(swap):
     A = make_matrix(40, 1000, "int2", seed=3200, device="cuda")

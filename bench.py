@@ -25,6 +25,7 @@ host cores on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -88,9 +89,13 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+    Samples count as "under load" when nvidia-smi's own timestamp falls inside
+    the wall-clock window bracketed by begin() / end() around the timed region
+    (utilization.gpu is a trailing average and lags a sub-second region)."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
@@ -98,15 +103,24 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.device_index = device_index
+        self.window = None
+        self._t0 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+
+    def begin(self):
+        self._t0 = datetime.datetime.now()
+
+    def end(self):
+        if self._t0 is not None:
+            self.window = (self._t0, datetime.datetime.now())
 
     def stop(self):
         if self.proc is None:
@@ -120,27 +134,39 @@ class ClockSampler:
         rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
+            if len(parts) < 11:
                 continue
             try:
-                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
-                             "util": float(parts[4]) if parts[4] not in ("", "[N/A]") else 0.0,
-                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
-                             "power_cap": parts[9]})
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                when = None
+            try:
+                rows.append({"t": when, "sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("", "[N/A]") else None,
+                             "hw": parts[7], "hw_thermal": parts[8], "sw_thermal": parts[9],
+                             "power_cap": parts[10]})
             except ValueError:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        loaded = [r for r in rows if r["util"] >= 50] or rows
+        in_window = []
+        if self.window:
+            lo, hi = self.window
+            in_window = [r for r in rows if r["t"] is not None and lo <= r["t"] <= hi]
+        loaded = in_window or rows
         reasons = set()
         for r in loaded:
             for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                               ("sw_thermal", "sw_thermal_slowdown"), ("power_cap", "sw_power_cap")):
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
+        powers = [r["power"] for r in loaded if r["power"] is not None]
         return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
                 "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
-                "samples": len(rows), "samples_under_load": len([r for r in rows if r["util"] >= 50])}
+                "samples": len(rows), "samples_under_load": len(in_window),
+                "power_w_median": statistics.median(powers) if powers else None,
+                "selection": ("samples timestamped inside the timed region" if in_window else
+                              "all samples (none fell inside the timed region)")}
 
 
 def input_sets(shape, device, l2_bytes, max_sets=4):
@@ -338,8 +364,10 @@ def run_ours(args):
     n0 = plan.launch_count()
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.2)
+    time.sleep(0.3)
+    sampler.begin()
     total_ms = time_region(ours, sets, args.steps, 0, stream, barrier)
+    sampler.end()
     clocks = sampler.stop()
     launches = plan.launch_count() - n0
     st = plan.status(stream)
@@ -470,7 +498,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=12000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--shape", default=HEADLINE)

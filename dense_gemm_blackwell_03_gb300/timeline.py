@@ -80,3 +80,43 @@ def summarize(trace: np.ndarray) -> dict:
         "tail_after_last_epilogue_us": _stat(tails),
         "units_per_cta": _stat([len(u) for u in per_unit]),
     }
+
+
+def main(argv=None) -> int:
+    """``python -m dense_gemm_blackwell_03_gb300.timeline --shape NAME``: trace
+    one launch of a named workload (after warm-up launches on rotating input
+    copies) and print its phase summary as JSON."""
+    import argparse
+    import json
+
+    import torch
+
+    from . import binding
+    from .workloads import SHAPES, make_inputs
+
+    ap = argparse.ArgumentParser(description=main.__doc__)
+    ap.add_argument("--shape", default="decode_attn_out", choices=sorted(SHAPES))
+    ap.add_argument("--schedule", type=int, default=0)
+    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=6)
+    args = ap.parse_args(argv)
+    s = SHAPES[args.shape]
+    sets = [make_inputs(s, device="cuda", seed=100 + i) for i in range(3)]
+    with binding.Plan(0, trace=1, schedule=args.schedule, split_k=args.split_k) as plan:
+        for i in range(args.warmup):
+            plan.gemm(*sets[i % 3])
+        torch.cuda.synchronize()
+        plan.gemm(*sets[0])
+        if plan.status() != 0:
+            raise SystemExit("device status error")
+        trace = plan.read_trace()
+        cfg = plan.last_config()
+    spans = [(u[1] - u[0]) / 1e3 for row in units(trace) for u in row if u[0] and u[1]]
+    out = {"shape": args.shape, "config": cfg, "summary": summarize(trace),
+           "mma_span_us_per_unit": _stat(spans)}
+    print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

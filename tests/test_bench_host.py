@@ -74,3 +74,43 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
                          timeout=120, cwd=ROOT, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi process: canned CSV lines."""
+
+    def __init__(self, text):
+        self.text = text
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.text, ""
+
+
+def test_clock_sampler_uses_samples_inside_the_timed_region():
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+    t0 = datetime.datetime(2026, 12, 2, 9, 0, 0)
+    lines = []
+    for i in range(10):  # every 100 ms; the region spans samples 3..6
+        t = t0 + datetime.timedelta(milliseconds=100 * i)
+        busy = 3 <= i <= 6
+        lines.append(", ".join([t.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3], "0",
+                                "1850" if busy else "2070", "2070", "1300.5" if busy else "200.0", "0",
+                                "0x4" if busy else "0x0", "Not Active", "Not Active", "Not Active",
+                                "Active" if busy else "Not Active"]))
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi("\n".join(lines))
+    s.window = (t0 + datetime.timedelta(milliseconds=250), t0 + datetime.timedelta(milliseconds=650))
+    c = s.stop()
+    assert c["samples"] == 10 and c["samples_under_load"] == 4
+    assert c["sm_mhz"] == 1850 and c["sm_max_mhz"] == 2070 and c["reasons"] == ["sw_power_cap"]
+    assert c["power_w_median"] == 1300.5
+    # no window (or none inside it): every sample is used and said so
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi("\n".join(lines))
+    c = s.stop()
+    assert c["samples_under_load"] == 0 and c["selection"].startswith("all samples")

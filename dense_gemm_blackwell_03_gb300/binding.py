@@ -69,7 +69,8 @@ class PlanOptions(ctypes.Structure):
         ("swap_ab", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
         ("copy_kblocks", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 1),
+        ("cluster_split", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -96,6 +97,7 @@ class Config(ctypes.Structure):
         ("copy_kblocks", ctypes.c_int32),
         ("prefetch_kblocks", ctypes.c_int32),
         ("prefetch_b", ctypes.c_int32),
+        ("cluster_split", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -65,8 +65,9 @@ struct KernelConfig {
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
-    // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4]
-    static constexpr int kNumBars = 2 * STAGES + 4 + 2 * kClcSlots;
+    // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4],
+    // exchange_ready, exchange_full
+    static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kClcSlots;
     static constexpr int kOffClcResp = kOffBar + kNumBars * 8;  // 16-byte responses
     static constexpr int kOffTmemSlot = kOffClcResp + 16 * kClcSlots;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -206,6 +207,7 @@ struct Sched {
     bool clc, first;
     int r;                    // next response to read
     int cs, mc, pair;         // CTAs per cluster, pairs per cluster, this CTA's pair
+    int ks;                   // K slices per tile inside the cluster (pair = slice)
     uint32_t resp, full, empty_leader;
 
     __device__ __forceinline__ void init(const GemmParams& p, int worker, int workers, int cs_,
@@ -216,6 +218,7 @@ struct Sched {
         cs = cs_;
         mc = mc_;
         pair = pair_;
+        ks = p.ks;
         clc = p.clc != 0;
         first = true;
         r = 0;
@@ -236,7 +239,15 @@ struct Sched {
         if (!clc) {
             if (!st.next(p, w))
                 return false;
-            w.n_blk = w.n_blk * mc + pair;
+            if (ks > 1) {
+                // the cluster's pairs take the K slices of one tile, in K order
+                w.split = pair;
+                w.kb0 = int((long long)pair * p.num_k_blocks / ks);
+                w.kb1 = int((long long)(pair + 1) * p.num_k_blocks / ks);
+                w.kind = kUnitSplit;
+            } else {
+                w.n_blk = w.n_blk * mc + pair;
+            }
             return true;
         }
         int tile;
@@ -483,7 +494,7 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
 // computes column block MC * n + i of the tile group (m, n); the CTAs with the
 // same rank in their pair need the same 128 A rows, so each loads 128 / MC of
 // them once from L2 and multicasts them to all MC.
-template <int CG, int BN, int STAGES, bool TR, int MC>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_a2,
@@ -491,7 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
     static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
-    constexpr int CS = CG * MC;  // CTAs per cluster
+    static_assert(KS == 1 || (KS == 2 && MC == 1), "a cluster holds column groups or K slices");
+    constexpr int CS = CG * MC * KS;  // CTAs per cluster
+    // K-slice exchange: each slice sends the other the 32-column chunks it owns,
+    // one [128 rows][32 fp32] block per chunk, into the other's idle A ring
+    constexpr int kXchgSlots = BN / kStoreCols / 2;
+    constexpr uint32_t kXchgBytes = uint32_t(kXchgSlots) * kRowsPerCta * kStoreCols * 4;
+    static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kABytes, "exchange fits the A ring");
+    static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kBBytes, "staging fits the B ring");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -515,6 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_acc_empty = bar_acc_full + 16;      // + 8 * buffer
     const uint32_t bar_clc_full = bar_acc_empty + 16;      // + 8 * slot
     const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots;  // + 8 * slot (leader's counts)
+    const uint32_t bar_xready = bar_clc_empty + 8 * kClcSlots;    // the other slice's ring is free
+    const uint32_t bar_xfull = bar_xready + 8;                    // the other slice's chunks landed
     const uint32_t clc_resp = base + Cfg::kOffClcResp;     // + 16 * slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
@@ -532,8 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kClcSlots; ++s) {
             ptx::mbar_init(bar_clc_full + 8 * s, 1);  // local producer's arrive.expect_tx(16)
             // readers of a response: producers and epilogue warps of every CTA, the MMA threads
-            ptx::mbar_init(bar_clc_empty + 8 * s, CS * (1 + kEpiWarps) + MC);
+            ptx::mbar_init(bar_clc_empty + 8 * s, CS * (1 + kEpiWarps) + CS / CG);
         }
+        ptx::mbar_init(bar_xready, 1);  // the partner's arrival
+        ptx::mbar_init(bar_xfull, 1);   // own arrive.expect_tx; the partner's st.async bytes
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -758,11 +780,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_f16<CG>(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc,
                                          (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
-                    // the stage is free once every pair sharing it has read it
+                    // the stage is free once every pair sharing it has read it (with
+                    // A multicast both pairs of the cluster, else this pair)
                     if constexpr (CG == 1)
                         ptx::mma_commit(bar_empty + 8 * stage);
-                    else
+                    else if constexpr (MC > 1)
                         ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t((1u << CS) - 1u));
+                    else
+                        ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t(0x3u << (CG * pair)));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -793,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* const parts = reinterpret_cast<float4*>(p.partials);
         int chunk_ctr = 0;
         int t = 0;
+        int xchg_count = 0;  // K-slice exchanges done (parity of the exchange barriers)
         Sched iter;
         iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
         WorkUnit w;
@@ -814,6 +840,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cta_row0 = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
             const int m_row = cta_row0 + q * 32;  // first row of this warp's boxes
             const int n_col = w.n_blk * BN;
+            if (KS > 1 && w.kind == kUnitSplit) {
+                // ---- split-K inside the cluster: the two K slices of this tile
+                // run on the two pairs (or CTAs) of the cluster.  Chunk c belongs
+                // to slice c % 2.  Each CTA stages the chunks its partner (same
+                // rank in the other slice) owns in its own idle B ring, tells the
+                // partner its A ring is free, and once the partner's is free
+                // bulk-copies the staged rows into it (counted on the partner's
+                // exchange barrier); then it waits for its own chunks and stores
+                // own + partner's in C.  One tile per
+                // cluster (the planner's one-wave rule), so no later unit
+                // refills the ring.  Warps whose rows are all past M take part
+                // too (the byte counts cover every row); their rows are clipped.
+                // (Per-thread st.async remote stores measured ~3 GB/s per warp;
+                // one 4 KiB bulk copy per warp and chunk is far faster.)
+                const int j = w.split;
+                const uint32_t partner = rank ^ uint32_t(CG);
+                const uint32_t xparity = uint32_t(xchg_count & 1);
+                ++xchg_count;
+                const uint32_t swz = uint32_t(row & 7);
+                auto xoff = [&](int c, int v) -> uint32_t {  // [slot][row][16-byte v ^ row % 8]
+                    return uint32_t((c >> 1) * (kRowsPerCta * kStoreCols * 4) + row * (kStoreCols * 4)) +
+                           ((uint32_t(v) ^ swz) << 4);
+                };
+                bool owns_any = false;
+                int last_owned = c_begin;
+#pragma unroll 1
+                for (int c = c_begin; c < c_end; ++c) {
+                    if (c % 2 == j) {
+                        owns_any = true;
+                        last_owned = c;
+                        continue;
+                    }
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        ptx::st_shared_v4(sB + xoff(c, v), r[4 * v + 0], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                }
+                if (!owns_any)
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
+                ptx::fence_proxy_async_smem();  // the staged rows, visible to the bulk copies
+                __syncwarp();
+                if (warp == 2 && lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar_xfull, kXchgBytes);
+                    ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
+                }
+                if (!__all_sync(0xffffffffu, wait_phase(bar_xready, xparity, p, abort_flag,
+                                                        kStatusSplitTimeout)))
+                    break;
+                if (lane == 0) {
+                    const uint32_t remote_ring = ptx::map_to_cta(sA, partner);
+                    const uint32_t remote_full = ptx::map_to_cta(bar_xfull, partner);
+                    constexpr uint32_t kWarpRows = 32 * kStoreCols * 4;  // this warp's 32 rows of a chunk
+                    for (int c = c_begin; c < c_end; ++c) {
+                        if (c % 2 == j)
+                            continue;
+                        const uint32_t off = uint32_t((c >> 1) * (kRowsPerCta * kStoreCols * 4) +
+                                                      q * 32 * (kStoreCols * 4));
+                        ptx::bulk_copy_to_cluster(remote_ring + off, sB + off, kWarpRows, remote_full);
+                    }
+                }
+                if (!__all_sync(0xffffffffu, wait_phase(bar_xfull, xparity, p, abort_flag,
+                                                        kStatusSplitTimeout)))
+                    break;
+#pragma unroll 1
+                for (int c = c_begin; c < c_end; ++c) {
+                    if (c % 2 != j)
+                        continue;
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                    uint32_t x[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        ptx::ld_shared_v4(sA + xoff(c, v), x[4 * v + 0], x[4 * v + 1], x[4 * v + 2],
+                                          x[4 * v + 3]);
+                    ptx::tmem_ld_wait();
+                    if (c == last_owned)
+                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
+                    // two terms: the sum is the same whichever slice adds
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(x[i]));
+                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                }
+                continue;
+            }
+
             if (m_row >= p.M) {
                 // every row of this warp is padding past M: nothing to load or store
                 // (the same holds for every piece of the tile, so no counter is used)

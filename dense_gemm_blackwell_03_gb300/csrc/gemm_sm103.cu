@@ -6,13 +6,13 @@ namespace bwgemm {
 
 namespace {
 
-template <int CG, int BN, int STAGES, bool TR, int MC>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p, int grid,
                        cudaStream_t stream, bool pdl)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -24,9 +24,9 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
-    if (CG * MC > 1) {
+    if (CG * MC * KS > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = CG * MC;
+        attr[n].val.clusterDim.x = CG * MC * KS;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
@@ -41,16 +41,16 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     return cudaLaunchKernelEx(&cfg, kernel, a, b, c, a2, b2, p);
 }
 
-template <int CG, int BN, int STAGES, bool TR, int MC>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 cudaError_t max_active_one(int* out)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    if (CG * MC == 1) {
+    if (CG * MC * KS == 1) {
         int per_sm = 0, dev = 0, sms = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads,
                                                             Cfg::kSmemBytes);
@@ -64,12 +64,12 @@ cudaError_t max_active_one(int* out)
         return cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CG * MC, 1, 1);
+    cfg.gridDim = dim3(CG * MC * KS, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG * MC;
+    attr[0].val.clusterDim.x = CG * MC * KS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -85,28 +85,29 @@ struct VariantFns {
     int smem_bytes;
 };
 
-#define BWGEMM_VARIANT(CG, BN, ST, TR, MC)                                  \
-    {&launch_one<CG, BN, ST, TR, MC>, &max_active_one<CG, BN, ST, TR, MC>, \
+#define BWGEMM_VARIANT(CG, BN, ST, TR, MC, KS)                                      \
+    {&launch_one<CG, BN, ST, TR, MC, KS>, &max_active_one<CG, BN, ST, TR, MC, KS>, \
      KernelConfig<CG, BN, ST>::kSmemBytes}
 
 // same order as kVariants in internal.h
 constexpr VariantFns kFns[] = {
-    BWGEMM_VARIANT(1, 256, 4, false, 1), BWGEMM_VARIANT(1, 128, 6, false, 1),
-    BWGEMM_VARIANT(2, 256, 6, false, 1), BWGEMM_VARIANT(2, 128, 8, false, 1),
-    BWGEMM_VARIANT(2, 128, 8, true, 1),  BWGEMM_VARIANT(2, 64, 9, true, 1),
-    BWGEMM_VARIANT(1, 128, 6, true, 1),  BWGEMM_VARIANT(1, 64, 8, true, 1),
-    BWGEMM_VARIANT(2, 256, 6, false, 2), BWGEMM_VARIANT(2, 128, 8, false, 2),
+    BWGEMM_VARIANT(1, 256, 4, false, 1, 1), BWGEMM_VARIANT(1, 128, 6, false, 1, 1),
+    BWGEMM_VARIANT(2, 256, 6, false, 1, 1), BWGEMM_VARIANT(2, 128, 8, false, 1, 1),
+    BWGEMM_VARIANT(2, 128, 8, true, 1, 1),  BWGEMM_VARIANT(2, 64, 9, true, 1, 1),
+    BWGEMM_VARIANT(1, 128, 6, true, 1, 1),  BWGEMM_VARIANT(1, 64, 8, true, 1, 1),
+    BWGEMM_VARIANT(2, 256, 6, false, 2, 1), BWGEMM_VARIANT(2, 128, 8, false, 2, 1),
+    BWGEMM_VARIANT(2, 256, 6, false, 1, 2), BWGEMM_VARIANT(1, 64, 8, true, 1, 2),
 };
 #undef BWGEMM_VARIANT
 static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");
 
 }  // namespace
 
-int find_variant(int cg, int bn, bool trans, int mc)
+int find_variant(int cg, int bn, bool trans, int mc, int ks)
 {
     for (int i = 0; i < kNumVariants; ++i)
         if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans &&
-            kVariants[i].mc == mc)
+            kVariants[i].mc == mc && kVariants[i].ks == ks)
             return i;
     return -1;
 }

@@ -12,27 +12,31 @@
 namespace bwgemm {
 
 // Compiled kernel variants: (CTA group, BN, ring stages, swapped operands,
-// pairs per cluster sharing A).  Every variant keeps the ring at <= 192 KiB of
-// shared memory plus 32 KiB of epilogue staging.  The swapped variants
-// compute C^T = B A^T for small M; the mc = 2 variants run clusters of two
-// CTA pairs on adjacent column blocks that multicast their common A tile.
+// pairs per cluster sharing A, K slices per cluster).  Every variant keeps the
+// ring at <= 192 KiB of shared memory plus 32 KiB of epilogue staging.  The
+// swapped variants compute C^T = B A^T for small M; the mc = 2 variants run
+// clusters of two CTA pairs on adjacent column blocks that multicast their
+// common A tile; the ks = 2 variants run the two K slices of a split-K tile
+// in one cluster and exchange partials through distributed shared memory.
 struct Variant {
     int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
     int bn;      // columns of the MMA per unit (= MMA N)
     int stages;  // shared-memory ring depth
     bool trans;  // operands swapped, accumulator holds C transposed
     int mc;      // CTA pairs per cluster sharing each A tile (1 = no multicast)
+    int ks;      // K slices of a tile per cluster (1, or 2 for the clustered split-K)
 };
 
 constexpr Variant kVariants[] = {
-    {1, 256, 4, false, 1}, {1, 128, 6, false, 1}, {2, 256, 6, false, 1}, {2, 128, 8, false, 1},
-    {2, 128, 8, true, 1},  {2, 64, 9, true, 1},   {1, 128, 6, true, 1},  {1, 64, 8, true, 1},
-    {2, 256, 6, false, 2}, {2, 128, 8, false, 2},
+    {1, 256, 4, false, 1, 1}, {1, 128, 6, false, 1, 1}, {2, 256, 6, false, 1, 1},
+    {2, 128, 8, false, 1, 1}, {2, 128, 8, true, 1, 1},  {2, 64, 9, true, 1, 1},
+    {1, 128, 6, true, 1, 1},  {1, 64, 8, true, 1, 1},   {2, 256, 6, false, 2, 1},
+    {2, 128, 8, false, 2, 1}, {2, 256, 6, false, 1, 2}, {1, 64, 8, true, 1, 2},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
 // Index into kVariants, or -1.
-int find_variant(int cg, int bn, bool trans, int mc = 1);
+int find_variant(int cg, int bn, bool trans, int mc = 1, int ks = 1);
 
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);

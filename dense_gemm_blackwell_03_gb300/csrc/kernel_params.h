@@ -77,6 +77,8 @@ struct GemmParams {
     int32_t k_chunks_a;     // whole 64-element K chunks the 3-D view of A covers
     int32_t k_chunks_b;     // (floor(K / 64)) and of B; 0: that view was not built
     int32_t pair_copies;    // 1: load two K blocks per copy where the 3-D views allow
+    int32_t ks;             // K slices of a tile inside one cluster (1, or 2: split-K whose
+                            // two slices exchange partials through distributed shared memory)
 };
 
 // Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).

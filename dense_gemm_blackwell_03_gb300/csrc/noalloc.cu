@@ -146,7 +146,8 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     bwgemm_default_options(&opts);
     opts.split_k = split_k;
     opts.swap_ab = 1;    // operands in the order given
-    opts.multicast = 1;  // one CTA pair per cluster: the scratch below is sized for it
+    opts.multicast = 1;      // one CTA pair per cluster: the scratch below is sized for it
+    opts.cluster_split = 1;  // slices reduce through the scratch array, not in a cluster
     Selection sel;
     // plan as if the workspace were unbounded, then hold the need against the array
     if ((st = select_config(ds->num_sms, ds->max_pairs, 0, M, N, K, opts, ~uint64_t(0), &sel)) !=

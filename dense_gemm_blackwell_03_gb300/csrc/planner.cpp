@@ -178,12 +178,33 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     // all slices of every tile in one wave: they may wait for one another
     const bool scatter = !stream_k && s > 1 && tiles * s <= slots;
 
+    // Two K slices of a tile inside one cluster (two pairs, or two CTAs),
+    // exchanging partials through distributed shared memory instead of L2:
+    // one-wave split-K with two slices, when a cluster per tile fits at once.
+    int idx_run = idx;
+    bool cluster_split = false;
+    if (opts.cluster_split < 0 || opts.cluster_split > 2)
+        return BWGEMM_ERR_INVALID_ARG;
+    if (opts.cluster_split != 1 && mc == 1 && scatter && s == 2 && !clc) {
+        const int ks_idx = find_variant(cg, bn, swap, 1, 2);
+        const int64_t ks_slots = (cg == 2) ? max_quads : max_pairs;  // clusters of 2 * cg CTAs
+        if (ks_idx >= 0 && tiles <= ks_slots && (opts.max_ctas == 0 || tiles * cg * 2 <= opts.max_ctas)) {
+            idx_run = ks_idx;
+            cluster_split = true;
+            workers = tiles;
+            ws = 0;  // no partials or counters in global memory
+        }
+    }
+    if (opts.cluster_split == 2 && !cluster_split)
+        return BWGEMM_ERR_UNSUPPORTED;
+    const int cs_run = cluster_split ? cg * 2 : cs;
+
     int64_t group = opts.raster_group > 0 ? opts.raster_group : 8;
     group = std::max<int64_t>(1, std::min<int64_t>(group, std::max<int64_t>(num_m, 1)));
 
     Selection sel;
     std::memset(&sel, 0, sizeof(sel));
-    sel.variant_idx = idx;
+    sel.variant_idx = idx_run;
     sel.swap = swap;
     sel.num_m_blocks = int(num_m);
     sel.num_n_blocks = int(num_n);
@@ -198,7 +219,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.raster_group = int32_t(group);
     sel.cfg.num_tiles = int32_t(tiles);
     sel.cfg.num_units = int32_t(dp_tiles * s);
-    sel.cfg.grid = int32_t(workers * cs);
+    sel.cfg.grid = int32_t(workers * cs_run);
     sel.cfg.workspace_bytes = ws;
     sel.cfg.schedule = clc ? BWGEMM_SCHEDULE_CLC
                            : (stream_k ? BWGEMM_SCHEDULE_STREAM_K : BWGEMM_SCHEDULE_TILES);
@@ -208,6 +229,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.split_scatter = scatter ? 1 : 0;
     sel.cfg.swap_ab = swap ? 1 : 0;
     sel.cfg.multicast = mc;
+    sel.cfg.cluster_split = cluster_split ? 1 : 0;
     // K blocks per operand copy.  Two (3-D copies) when the kernel is compute
     // bound: one TMA copy occupies its unit for ~140 ns whatever its size, and
     // two 16 KiB copies per K block take longer than the K block's MMAs.  In
@@ -252,6 +274,14 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
     p.prefetch = sel.cfg.prefetch_kblocks;
     p.prefetch_b = sel.cfg.prefetch_b;
     p.clc = sel.cfg.schedule == BWGEMM_SCHEDULE_CLC ? 1 : 0;
+    p.ks = 1;
+    if (sel.cfg.cluster_split) {
+        // the cluster walks whole tiles; its pairs take the K slices
+        p.ks = sel.cfg.split_k;
+        p.split_k = 1;
+        p.dp_units = sel.cfg.num_tiles;
+        p.split_scatter = 0;
+    }
     return p;
 }
 

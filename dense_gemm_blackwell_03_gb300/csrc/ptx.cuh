@@ -222,6 +222,27 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t 
                  : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into another CTA's (mapa address); the bytes
+// are counted on that CTA's mbarrier `remote_bar`.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t remote_dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t remote_bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            remote_dst),
+        "r"(src), "r"(bytes), "r"(remote_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d)
+{
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(addr)
+                 : "memory");
+}
+
 // Prefetch one 3-D box (two K chunks of the 3-D operand views) into L2.
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2)
 {

@@ -104,7 +104,11 @@ typedef struct {
     int32_t copy_kblocks;     /* K blocks per TMA operand copy: 0 = auto (two for
                                  compute-bound shapes), 1 = one, 2 = two (where K holds
                                  at least two whole 64-element chunks)                   */
-    int32_t reserved[1];      /* must be zero                                            */
+    int32_t cluster_split;    /* 0 = auto, 1 = off, 2 = required: the two K slices of a
+                                 one-wave split-K tile run in one cluster and exchange
+                                 partials through distributed shared memory (when a
+                                 cluster per tile fits at once)                          */
+    int32_t reserved[2];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -136,6 +140,8 @@ typedef struct {
                              where K holds at least two whole 64-element chunks) */
     int32_t prefetch_kblocks; /* L2 prefetch distance of the streamed operand (0: off) */
     int32_t prefetch_b;   /* the streamed operand: 1 = B (the kernel's), 0 = A   */
+    int32_t cluster_split; /* 1: split_k = 2 slices per tile inside one cluster,
+                              partials exchanged in distributed shared memory    */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

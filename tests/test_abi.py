@@ -217,6 +217,24 @@ def test_select_multicast_pairs_of_pairs():
     assert cfg(4096, 4096, 4096, copy_kblocks=1)["copy_kblocks"] == 1
 
 
+def test_select_cluster_split():
+    # one-wave split-K with two slices: the slices of a tile share a cluster
+    c = cfg(256, 8192, 8192, sms=152, pairs=76)
+    assert c["cluster_split"] == 1 and c["split_k"] == 2 and c["grid"] == 32 * 4
+    assert c["workspace_bytes"] == 0
+    c = cfg(16, 8192, 8192, sms=152, pairs=76)  # swapped: clusters of two single CTAs
+    assert c["swap_ab"] == 1 and c["cluster_split"] == 1 and c["grid"] == 64 * 2
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, cluster_split=1)
+    assert c["cluster_split"] == 0 and c["split_scatter"] == 1 and c["workspace_bytes"] > 0
+    # 40 tiles need 40 clusters of four CTAs: more than fit at once
+    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    assert c["cluster_split"] == 0
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 10240, 8192, sms=152, pairs=76, cluster_split=2)
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 8192, 8192, cluster_split=3)
+
+
 def test_select_prefetch():
     c = cfg(256, 8192, 8192, sms=152, pairs=76)
     assert c["prefetch_kblocks"] == 0 and c["prefetch_b"] == 1  # off unless asked for
@@ -240,10 +258,11 @@ def test_select_kblocks_per_copy():
 
 
 def test_select_tiles_schedule_splits_k():
-    c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1)
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1,
+            cluster_split=1)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2
     assert c["num_units"] == 64 and c["grid"] == 128 and c["split_scatter"] == 1
-    assert c["workspace_bytes"] == (1 << 20) + 32 * 2 * 2 * 128 * 256 * 4
+    assert c["workspace_bytes"] == (1 << 20) + 32 * 2 * 2 * 128 * 256 * 4  # partials through L2
     # more slices than one wave holds: no reduce-scatter (slices may not wait)
     c = cfg(256, 8192, 8192, sms=152, pairs=76, split_k=3, swap_ab=1)
     assert c["split_k"] == 3 and c["split_scatter"] == 0

@@ -238,6 +238,34 @@ def test_paired_kblock_copies_swapped(swap):
         assert p.last_config()["swap_ab"] == 1 and p.last_config()["copy_kblocks"] == 2
 
 
+# ------------------------------ split-K slices exchanging in distributed shared memory
+@pytest.mark.parametrize("M,N,K", [(256, 2048, 1024), (200, 2048, 1000), (130, 1024, 520),
+                                   (16, 4096, 512), (40, 2048, 1088), (1, 2048, 640)])
+def test_cluster_split_exact(M, N, K):
+    # two K slices of each tile in one cluster against the same split through
+    # L2: identical bits (a sum of two terms); padding rows past M take part
+    A = make_matrix(M, K, "int2", seed=3400 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=3500 + N, device="cuda")
+    outs = []
+    for mode in (1, 2):
+        with binding.Plan(0, split_k=2, cluster_split=mode, schedule=binding.SCHEDULE_TILES) as p:
+            for _ in range(2):
+                _, C = run_full(p, A, B, "bf16", exact=True)
+            c = p.last_config()
+            assert c["cluster_split"] == (1 if mode == 2 else 0) and c["split_k"] == 2
+            outs.append(C.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_cluster_split_normal_inputs(dtype):
+    A = make_matrix(256, 4096, "normal", dtype, seed=3600, device="cuda")
+    B = make_matrix(3072, 4096, "weight", dtype, seed=3601, device="cuda")
+    with binding.Plan(0, cluster_split=2, split_k=2, schedule=binding.SCHEDULE_TILES) as p:
+        run_full(p, A, B, dtype)
+        assert p.last_config()["cluster_split"] == 1
+
+
 # ------------------------------------------------- A multicast across two pairs
 @pytest.mark.parametrize("M,N,K", [(512, 1024, 192), (300, 768, 200), (1000, 1300, 520),
                                    (256, 256, 64)])

@@ -36,7 +36,7 @@ EXPORTED = [
     "bwgemm_run_host", "bwgemm_get_status", "bwgemm_last_device_status", "bwgemm_check_args",
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
     "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
-    "bwgemm_plan_read_trace",
+    "bwgemm_plan_read_trace", "bwgemm_tune", "bwgemm_plan_tuned_count",
 ]
 
 # timeline slots of bwgemm_plan_read_trace
@@ -160,6 +160,10 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_plan_read_trace.restype = st
         lib.bwgemm_plan_launch_count.argtypes = [vp]
         lib.bwgemm_plan_launch_count.restype = ctypes.c_uint64
+        lib.bwgemm_tune.argtypes = gemm_args + [i32, ctypes.POINTER(Config)]
+        lib.bwgemm_tune.restype = st
+        lib.bwgemm_plan_tuned_count.argtypes = [vp]
+        lib.bwgemm_plan_tuned_count.restype = i32
         lib.bwgemm_status_string.argtypes = [ctypes.c_int]
         lib.bwgemm_status_string.restype = ctypes.c_char_p
         lib.bwgemm_version.argtypes = []
@@ -313,6 +317,29 @@ class Plan:
 
     def launch_count(self) -> int:
         return int(self.lib.bwgemm_plan_launch_count(self.handle))
+
+    def tune(self, A, B, out=None, iters: int = 10, stream=None) -> dict:
+        """``bwgemm_tune``: time the candidate configurations on A, B, out and
+        keep the fastest for this shape; returns its configuration.  `out`
+        holds the product afterwards."""
+        import torch
+        dt = _dtype_code(A)
+        if B.dtype != A.dtype or not (A.is_cuda and B.is_cuda):
+            raise ValueError("A and B must be CUDA tensors of one dtype")
+        M, K = A.shape
+        N, _ = B.shape
+        if out is None:
+            out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+        cfg = Config()
+        rc = self.lib.bwgemm_tune(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                                  _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream), int(iters),
+                                  ctypes.byref(cfg))
+        if rc != 0:
+            raise BwgemmError(rc, "bwgemm_tune")
+        return cfg.as_dict()
+
+    def tuned_count(self) -> int:
+        return int(self.lib.bwgemm_plan_tuned_count(self.handle))
 
     def read_trace(self):
         """Timeline of the last launch (plan created with trace=1): a

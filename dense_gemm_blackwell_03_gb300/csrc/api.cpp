@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -164,13 +165,31 @@ struct bwgemm_plan_s {
     uint64_t* d_trace = nullptr;
     int trace_ctas = 0;
     int last_grid = 0;
+    // options chosen by bwgemm_tune, per shape; bwgemm_run uses them for that shape
+    struct Tuned {
+        int64_t M, N, K;
+        int dtype;
+        bwgemm_plan_options_t opts;
+    };
+    std::vector<Tuned> tuned;
 };
 
 namespace {
 
-bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
-                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                        bwgemm_dtype_t dtype, cudaStream_t stream)
+// The options bwgemm_run uses for a shape: the tuned ones if bwgemm_tune
+// recorded some, else the plan's.
+const bwgemm_plan_options_t& options_for(bwgemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                                         bwgemm_dtype_t dtype)
+{
+    for (const auto& t : plan->tuned)
+        if (t.M == M && t.N == N && t.K == K && t.dtype == int(dtype))
+            return t.opts;
+    return plan->opts;
+}
+
+bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, const void* A,
+                        const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                        int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, cudaStream_t stream)
 {
     bwgemm_status_t st = bwgemm_check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype);
     if (st != BWGEMM_OK)
@@ -184,7 +203,7 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     }
     Selection sel;
     st = select_config(plan->num_sms, plan->max_active[find_variant(2, 256, false, 1)],
-                       plan->max_active[find_variant(2, 256, false, 2)], M, N, K, plan->opts,
+                       plan->max_active[find_variant(2, 256, false, 2)], M, N, K, opts,
                        plan->workspace_bytes, &sel);
     if (st != BWGEMM_OK)
         return st;
@@ -222,13 +241,13 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     p.k_chunks_a = view_a ? int32_t(chunks) : 0;
     p.k_chunks_b = view_b ? int32_t(chunks) : 0;
     p.pair_copies = pair_copies ? 1 : 0;
-    p.timeout_ns = plan->opts.timeout_ns ? plan->opts.timeout_ns : 4000000000ull;
+    p.timeout_ns = opts.timeout_ns ? opts.timeout_ns : 4000000000ull;
     p.status = plan->d_status;
     p.c = static_cast<uint16_t*>(C);
     p.ldc = ldc;
     p.tile_sems = reinterpret_cast<uint32_t*>(plan->d_workspace);
     p.partials = reinterpret_cast<float*>(plan->d_workspace + kCounterRegionBytes);
-    p.stall_kblock = plan->opts.stall_kblock;
+    p.stall_kblock = opts.stall_kblock;
     if (plan->d_trace) {
         if (sel.cfg.grid > plan->trace_ctas)
             return BWGEMM_ERR_UNSUPPORTED;
@@ -242,7 +261,7 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const void* A, const void* B, void* 
     const CUtensorMap& b2 = view_b ? plan->tmaps[4].map : plan->tmaps[1].map;
     const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
                                            plan->tmaps[2].map, a2, b2, p, sel.cfg.grid, stream,
-                                           plan->opts.pdl_off == 0);
+                                           opts.pdl_off == 0);
     if (err != cudaSuccess)
         return BWGEMM_ERR_CUDA;
     plan->last = sel.cfg;
@@ -367,7 +386,8 @@ bwgemm_status_t bwgemm_run(bwgemm_plan_t plan, const void* A, const void* B, voi
     DeviceGuard guard(plan->device);
     if (!guard.ok)
         return BWGEMM_ERR_CUDA;
-    return enqueue(plan, A, B, C, M, N, K, lda, ldb, ldc, dtype, static_cast<cudaStream_t>(stream));
+    return enqueue(plan, options_for(plan, M, N, K, dtype), A, B, C, M, N, K, lda, ldb, ldc, dtype,
+                   static_cast<cudaStream_t>(stream));
 }
 
 bwgemm_status_t bwgemm_get_status(bwgemm_plan_t plan, void* stream)
@@ -435,7 +455,8 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
             copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice) != cudaSuccess)
             return BWGEMM_ERR_CUDA;
     }
-    st = enqueue(plan, plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N, K, dlda, dlda, dldc, dtype, s);
+    st = enqueue(plan, options_for(plan, M, N, K, dtype), plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N,
+                 K, dlda, dlda, dldc, dtype, s);
     if (st != BWGEMM_OK)
         return st;
     if (copy_rows(C_host, ldc, plan->h2d[2], dldc, N, M, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -450,6 +471,123 @@ bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out
     *out = plan->last;
     return BWGEMM_OK;
 }
+
+bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                            bwgemm_dtype_t dtype, void* stream, int32_t iters, bwgemm_config_t* best)
+{
+    if (!plan || iters <= 0 || iters > 10000)
+        return BWGEMM_ERR_INVALID_ARG;
+    bwgemm_status_t st = bwgemm_check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype);
+    if (st != BWGEMM_OK)
+        return st;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok)
+        return BWGEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // Candidates: the plan's options with one or two choices overridden.  Each
+    // is planned on the host first; ones that fail to plan or plan to a
+    // configuration already seen are skipped.
+    struct Override {
+        int32_t variant, tile_n, split_k, schedule, copy_kblocks, cluster_split, raster_group, swap_ab;
+    };
+    const Override kCandidates[] = {
+        {-1, -1, -1, -1, -1, -1, -1, -1},  // the plan's own choice
+        {-1, -1, 1, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
+        {-1, -1, -1, BWGEMM_SCHEDULE_STREAM_K, -1, -1, -1, -1},
+        {-1, -1, 2, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
+        {-1, -1, 3, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
+        {-1, -1, 4, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
+        {-1, -1, -1, -1, 1, -1, -1, -1},
+        {-1, -1, -1, -1, 2, -1, -1, -1},
+        {-1, -1, -1, -1, -1, 1, -1, -1},
+        {-1, 128, -1, -1, -1, -1, -1, -1},
+        {BWGEMM_VARIANT_1SM, -1, -1, -1, -1, -1, -1, -1},
+        {BWGEMM_VARIANT_1SM, 128, -1, -1, -1, -1, -1, -1},
+        {-1, -1, -1, -1, -1, -1, 4, -1},
+        {-1, -1, -1, -1, -1, -1, 16, -1},
+        {-1, -1, -1, -1, -1, -1, -1, 1},
+        {-1, -1, -1, -1, -1, -1, -1, 2},
+        {-1, -1, -1, BWGEMM_SCHEDULE_CLC, -1, -1, -1, -1},
+    };
+    const int pairs = plan->max_active[find_variant(2, 256, false, 1)];
+    const int quads = plan->max_active[find_variant(2, 256, false, 2)];
+    std::vector<bwgemm_plan_options_t> cands;
+    std::vector<bwgemm_config_t> cfgs;
+    for (const Override& o : kCandidates) {
+        bwgemm_plan_options_t opts = plan->opts;
+        opts.trace = 0;
+        opts.stall_kblock = -1;
+        if (o.variant >= 0) opts.variant = o.variant;
+        if (o.tile_n >= 0) opts.tile_n = o.tile_n;
+        if (o.split_k >= 0) opts.split_k = o.split_k;
+        if (o.schedule >= 0) opts.schedule = o.schedule;
+        if (o.copy_kblocks >= 0) opts.copy_kblocks = o.copy_kblocks;
+        if (o.cluster_split >= 0) opts.cluster_split = o.cluster_split;
+        if (o.raster_group >= 0) opts.raster_group = o.raster_group;
+        if (o.swap_ab >= 0) opts.swap_ab = o.swap_ab;
+        Selection sel;
+        if (select_config(plan->num_sms, pairs, quads, M, N, K, opts, plan->workspace_bytes, &sel) != BWGEMM_OK)
+            continue;
+        bool seen = false;
+        for (const auto& c : cfgs)
+            seen = seen || std::memcmp(&c, &sel.cfg, sizeof(c)) == 0;
+        if (seen)
+            continue;
+        cands.push_back(opts);
+        cfgs.push_back(sel.cfg);
+    }
+    if (cands.empty())
+        return BWGEMM_ERR_UNSUPPORTED;
+
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0)
+            cudaEventDestroy(e0);
+        return BWGEMM_ERR_CUDA;
+    }
+    int best_i = -1;
+    float best_ms = 0.f;
+    for (size_t i = 0; i < cands.size(); ++i) {
+        bool ok = true;
+        for (int w = 0; w < 2 && ok; ++w)
+            ok = enqueue(plan, cands[i], A, B, C, M, N, K, lda, ldb, ldc, dtype, s) == BWGEMM_OK;
+        ok = ok && cudaEventRecord(e0, s) == cudaSuccess;
+        for (int w = 0; w < iters && ok; ++w)
+            ok = enqueue(plan, cands[i], A, B, C, M, N, K, lda, ldb, ldc, dtype, s) == BWGEMM_OK;
+        ok = ok && cudaEventRecord(e1, s) == cudaSuccess;
+        // a candidate whose launches reported a device-side error is not kept
+        ok = ok && bwgemm_get_status(plan, stream) == BWGEMM_OK;
+        float ms = 0.f;
+        if (ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && (best_i < 0 || ms < best_ms)) {
+            best_i = int(i);
+            best_ms = ms;
+        }
+        cudaGetLastError();
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (best_i < 0)
+        return BWGEMM_ERR_CUDA;
+
+    bool replaced = false;
+    for (auto& t : plan->tuned)
+        if (t.M == M && t.N == N && t.K == K && t.dtype == int(dtype)) {
+            t.opts = cands[best_i];
+            replaced = true;
+        }
+    if (!replaced)
+        plan->tuned.push_back({M, N, K, int(dtype), cands[best_i]});
+    // leave C holding the chosen configuration's result
+    if ((st = enqueue(plan, cands[best_i], A, B, C, M, N, K, lda, ldb, ldc, dtype, s)) != BWGEMM_OK)
+        return st;
+    if (best)
+        *best = cfgs[best_i];
+    return BWGEMM_OK;
+}
+
+int32_t bwgemm_plan_tuned_count(bwgemm_plan_t plan) { return plan ? int32_t(plan->tuned.size()) : 0; }
 
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan) { return plan ? plan->launches : 0u; }
 

@@ -241,6 +241,29 @@ bwgemm_status_t bwgemm_plan_read_trace(bwgemm_plan_t plan, uint64_t* out, int64_
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);
 
 /*
+ * Shape-keyed tuning ("Matrix Multiplication on NVIDIA's Blackwell", the
+ * Gemma-shape experiment, chooses pipeline and MMA shapes per shape with an
+ * autotuner).  Times a fixed list of candidate configurations -- the plan's
+ * options with the schedule, split-K slices, variant, tile width, K blocks
+ * per copy, clustered split, raster group or operand order overridden -- on
+ * the caller's A, B and C (the same arguments and rules as bwgemm_run), each
+ * for `iters` launches (1..10000) after two warm-up launches, timed with CUDA
+ * events on `stream`.  Candidates that fail to plan, plan to a configuration
+ * already tried, or report a device-side error are skipped.  The fastest is
+ * recorded in the plan for this (M, N, K, dtype): later bwgemm_run /
+ * bwgemm_run_host calls with that shape use it.  C is left holding the
+ * chosen configuration's result (every candidate computes the same C).
+ * Synchronises `stream`.  *best (may be NULL) receives the chosen
+ * configuration.  Not thread-safe with other calls on the same plan.
+ */
+bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                            bwgemm_dtype_t dtype, void* stream, int32_t iters, bwgemm_config_t* best);
+
+/* Number of shapes the plan holds tuned options for. */
+int32_t bwgemm_plan_tuned_count(bwgemm_plan_t plan);
+
+/*
  * C = A * B^T with split-K, allocating no device memory (the source pages
  * have no counterpart to this entry point).
  *

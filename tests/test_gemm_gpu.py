@@ -238,6 +238,37 @@ def test_paired_kblock_copies_swapped(swap):
         assert p.last_config()["swap_ab"] == 1 and p.last_config()["copy_kblocks"] == 2
 
 
+# ------------------------------------------------------------------ tuning
+def test_tune_keeps_a_valid_config_per_shape():
+    A = make_matrix(520, 1000, "int2", seed=3700, device="cuda")
+    B = make_matrix(696, 1000, "int2", seed=3701, device="cuda")
+    C = torch.full((520, 696), 5.0, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0) as p:
+        best = p.tune(A, B, out=C, iters=3)
+        assert p.tuned_count() == 1 and best["grid"] > 0
+        ref = oracle.gemm(bits_of(A), bits_of(B), "bf16")
+        compare(bits_of(C), ref, "bf16", 1000, exact=True)  # C holds the product
+        # later runs of this shape use the tuned configuration
+        run_full(p, A, B, "bf16", exact=True)
+        got = p.last_config()
+        assert {k: got[k] for k in best} == best
+        # another shape is not affected; re-tuning replaces the entry
+        A2 = make_matrix(256, 512, "int2", seed=3702, device="cuda")
+        run_full(p, A2, B[:, :512].contiguous(), "bf16", exact=True)
+        p.tune(A, B, out=C, iters=2)
+        assert p.tuned_count() == 1
+
+
+def test_tune_rejects_bad_arguments():
+    A = make_matrix(64, 64, "int2", seed=3703, device="cuda")
+    with binding.Plan(0) as p:
+        with pytest.raises(binding.BwgemmError):
+            p.tune(A, A, iters=0)
+        C = torch.empty((64, 60), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(binding.BwgemmError):
+            p.tune(A, A[:60].contiguous(), out=C[:, :60], iters=1)  # ldc 60: misaligned
+
+
 # ------------------------------ split-K slices exchanging in distributed shared memory
 @pytest.mark.parametrize("M,N,K", [(256, 2048, 1024), (200, 2048, 1000), (130, 1024, 520),
                                    (16, 4096, 512), (40, 2048, 1088), (1, 2048, 640)])
@@ -426,9 +457,13 @@ FULL = ["square4096", "square4096_fp16", "prefill_attn_out", "prefill_mlp_up",
         "gemma_512x8192x5376", "tail_m1", "tail_m16", "tail_m64", "tail_m200"]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_shape_sampled(plan, name):
-    s = SHAPES[name]
+FULL_FP16 = [n for n in FULL if not n.endswith("_fp16")]
+
+
+@pytest.mark.parametrize("name,dtype", [(n, None) for n in FULL] + [(n, "fp16") for n in FULL_FP16])
+def test_full_shape_sampled(plan, name, dtype):
+    # every configuration of the pages' shapes, in bf16 and in fp16
+    s = SHAPES[name] if dtype is None else SHAPES[name].with_dtype(dtype)
     A, B = make_inputs(s, device="cuda")
     C = plan.gemm(A, B)
     assert plan.status() == 0

@@ -425,16 +425,23 @@ def run_ours(args):
     # the pages' other shapes, timed alongside (not the headline)
     shapes = {}
     if not args.no_extra:
+        def steady(fn, ssets):
+            """Seconds per step: a pilot sizes blocks of about 0.1 s; after a
+            block of warm-up, the median of three timed blocks."""
+            pilot = time_region(fn, ssets, 10, 5, stream) / 1e3 / 10
+            it = int(min(5000, max(50, 0.1 / max(pilot, 1e-7))))
+            time_region(fn, ssets, it, 0, stream)
+            return statistics.median(time_region(fn, ssets, it, 0, stream) / 1e3 / it for _ in range(3))
+
         for name in EXTRA_SHAPES:
             s = SHAPES[name]
             ssets = input_sets(s, device, l2_bytes, max_sets=3)
-            it = 100
-            t = time_region(ours, ssets, it, 5, stream) / 1e3 / it
+            t = steady(ours, ssets)
             if plan.status(stream) != 0:
                 raise SystemExit(f"device status error on {name}")
             cfg = plan.last_config()
             med = statistics.median(time_each(ours, ssets, 50, stream)) / 1e3
-            t_cb = time_region(cublas, ssets, it, 5, stream) / 1e3 / it
+            t_cb = steady(cublas, ssets)
             r = roofline_entry(s, t, peaks)
             shapes[name] = {"M": s.M, "N": s.N, "K": s.K, "dtype": s.dtype,
                             "us": round(t * 1e6, 2), "median_us": round(med * 1e6, 2),

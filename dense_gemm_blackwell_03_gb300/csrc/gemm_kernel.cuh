@@ -66,13 +66,16 @@ struct KernelConfig {
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
     // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4],
-    // exchange_ready, exchange_full
-    static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kClcSlots;
-    static constexpr int kOffClcResp = kOffBar + kNumBars * 8;  // 16-byte responses
+    // exchange_ready, exchange_full, exchange_staged
+    static constexpr int kNumBars = 2 * STAGES + 7 + 2 * kClcSlots;
+    // 16-byte responses on 16-byte boundaries (the barrier count may be odd)
+    static constexpr int kOffClcResp = (kOffBar + kNumBars * 8 + 15) & ~15;
     static constexpr int kOffTmemSlot = kOffClcResp + 16 * kClcSlots;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1 KiB
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+    static_assert(kOffStore % 128 == 0 && kOffBar % 8 == 0 && kOffClcResp % 16 == 0,
+                  "store boxes need 128-byte, mbarriers 8-byte, launch-control responses 16-byte alignment");
     static_assert(kSmemBytes <= 227 * 1024, "exceeds the 227 KiB shared memory of one CTA");
     // floats of one CTA's fp32 partial tile
     static constexpr int kPartialFloats = kRowsPerCta * BN;
@@ -193,6 +196,26 @@ __device__ __forceinline__ void trace_unit(const GemmParams& p, int unit, int wh
             ptx::global_timer_ns();
 }
 
+// Time spent in one bounded wait.  %globaltimer is not guaranteed to move
+// forward smoothly (the driver may re-synchronise it with the host clock), and
+// a plain `now - start` in unsigned arithmetic would turn a step backwards
+// into an immediate timeout.  So only forward steps count, each capped at
+// 1 ms, and every poll counts at least 16 ns: a jump of the timer neither ends
+// a wait early nor stretches it, and the wait ends even if the timer stops.
+struct WaitClock {
+    uint64_t last;
+    uint64_t spent = 0;
+    __device__ __forceinline__ WaitClock() : last(ptx::global_timer_ns()) {}
+    __device__ __forceinline__ bool expired(uint64_t limit)
+    {
+        const uint64_t now = ptx::global_timer_ns();
+        const int64_t step = int64_t(now - last);
+        last = now;
+        spent += uint64_t(step < 16 ? 16 : (step > 1000000 ? 1000000 : step));
+        return spent > limit;
+    }
+};
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const GemmParams& p,
                                            volatile uint32_t* abort_flag, uint32_t code);
 
@@ -297,14 +320,14 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 {
     if (ptx::mbar_try_wait(bar, parity))
         return true;
-    const uint64_t t0 = ptx::global_timer_ns();
+    WaitClock clock;
 #pragma unroll 1
     while (true) {
         if (ptx::mbar_try_wait(bar, parity))
             return true;
         if (*abort_flag)
             return false;
-        if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
+        if (clock.expired(p.timeout_ns)) {
             atomicOr(p.status, code);
             *abort_flag = 1u;
             return false;
@@ -319,7 +342,7 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t want,
 {
     if (ptx::ld_acquire_gpu(ctr) == want)
         return true;
-    const uint64_t t0 = ptx::global_timer_ns();
+    WaitClock clock;
 #pragma unroll 1
     while (true) {
         __nanosleep(64);
@@ -327,7 +350,7 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t want,
             return true;
         if (*abort_flag)
             return false;
-        if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
+        if (clock.expired(p.timeout_ns)) {
             atomicOr(p.status, kStatusSplitTimeout);
             *abort_flag = 1u;
             return false;
@@ -342,7 +365,7 @@ __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint3
 {
     if (ptx::ld_acquire_gpu(ctr) >= want)
         return true;
-    const uint64_t t0 = ptx::global_timer_ns();
+    WaitClock clock;
 #pragma unroll 1
     while (true) {
         __nanosleep(32);
@@ -350,7 +373,7 @@ __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint3
             return true;
         if (*abort_flag)
             return false;
-        if (ptx::global_timer_ns() - t0 > p.timeout_ns) {
+        if (clock.expired(p.timeout_ns)) {
             atomicOr(p.status, kStatusSplitTimeout);
             *abort_flag = 1u;
             return false;
@@ -535,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots;  // + 8 * slot (leader's counts)
     const uint32_t bar_xready = bar_clc_empty + 8 * kClcSlots;    // the other slice's ring is free
     const uint32_t bar_xfull = bar_xready + 8;                    // the other slice's chunks landed
+    const uint32_t bar_xstaged = bar_xfull + 8;                   // every epilogue warp staged its rows
     const uint32_t clc_resp = base + Cfg::kOffClcResp;     // + 16 * slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
@@ -555,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_clc_empty + 8 * s, CS * (1 + kEpiWarps) + CS / CG);
         }
         ptx::mbar_init(bar_xready, 1);  // the partner's arrival
-        ptx::mbar_init(bar_xfull, 1);   // own arrive.expect_tx; the partner's st.async bytes
+        ptx::mbar_init(bar_xfull, 1);   // own arrive.expect_tx; the partner's bulk-copy bytes
+        ptx::mbar_init(bar_xstaged, kEpiWarps);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -581,12 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     // Everything above may overlap the previous kernel on the stream
-    // (programmatic dependent launch); nothing below touches global memory
-    // before that kernel has completed.  Then let the next kernel be scheduled.
-    ptx::grid_dependency_wait();
+    // (programmatic dependent launch), and so may each role's set-up below:
+    // every role waits for that kernel to complete (griddepcontrol.wait) just
+    // before its first access to global memory.  The next kernel may be
+    // scheduled from here on.
     ptx::launch_dependents();
-    if (threadIdx.x == 0)
-        trace_mark(p, kTraceReady);
     const uint32_t clc_empty_leader = (CS > 1) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
 
     if (warp == 0) {
@@ -607,6 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both CTAs' bytes of a pair are counted on the pair leader's barrier
         const uint32_t leader_full = (CG == 2) ? ptx::map_to_cta(bar_full, leader) : bar_full;
         while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusProducerTimeout)) {
+            if (first_unit) {
+                // the first unit is known; now wait for the previous kernel
+                ptx::grid_dependency_wait();
+                if (lane == 0)
+                    trace_mark(p, kTraceReady);
+            }
             if (p.clc) {
                 // ask for the tile after this one now, a whole tile ahead of need
                 const int rq = requested++;
@@ -746,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0 && prank == 0) {
+            ptx::grid_dependency_wait();
             const uint32_t idesc = p.idesc;
             const uint64_t a_desc0 = make_sdesc_sw128(sA);
             const uint64_t b_desc0 = make_sdesc_sw128(sB);
@@ -806,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         // Warps 2..9: two per TMEM lane quarter q (= warp % 4, the quarter a
         // warp may access); h selects the half of the columns it handles.
+        ptx::grid_dependency_wait();
         const int ew = warp - 2;
         const int q = warp & 3;
         const int h = ew >> 2;
@@ -844,16 +876,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- split-K inside the cluster: the two K slices of this tile
                 // run on the two pairs (or CTAs) of the cluster.  Chunk c belongs
                 // to slice c % 2.  Each CTA stages the chunks its partner (same
-                // rank in the other slice) owns in its own idle B ring, tells the
-                // partner its A ring is free, and once the partner's is free
-                // bulk-copies the staged rows into it (counted on the partner's
-                // exchange barrier); then it waits for its own chunks and stores
-                // own + partner's in C.  One tile per
-                // cluster (the planner's one-wave rule), so no later unit
-                // refills the ring.  Warps whose rows are all past M take part
-                // too (the byte counts cover every row); their rows are clipped.
-                // (Per-thread st.async remote stores measured ~3 GB/s per warp;
-                // one 4 KiB bulk copy per warp and chunk is far faster.)
+                // rank in the other slice) owns in its own idle B ring (one
+                // contiguous block); once every epilogue warp has staged its rows,
+                // one thread tells the partner that this CTA's A ring is free and,
+                // once the partner's is free, copies the whole block into it with
+                // one bulk copy (counted on the partner's exchange barrier); then
+                // every warp waits for its own chunks and stores own + partner's
+                // in C.  One tile per cluster (the planner's one-wave rule), so no
+                // later unit refills the ring.  Warps whose rows are all past M
+                // take part too (the byte counts cover every row); their rows are
+                // clipped.  (Per-thread st.async remote stores measured ~3 GB/s
+                // per warp; a bulk copy per warp and chunk was fast but each copy
+                // occupies the SM's TMA unit about as long as an operand load.)
                 const int j = w.split;
                 const uint32_t partner = rank ^ uint32_t(CG);
                 const uint32_t xparity = uint32_t(xchg_count & 1);
@@ -881,26 +915,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!owns_any)
                     release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
-                ptx::fence_proxy_async_smem();  // the staged rows, visible to the bulk copies
+                ptx::fence_proxy_async_smem();  // the staged rows, visible to the bulk copy
                 __syncwarp();
-                if (warp == 2 && lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar_xfull, kXchgBytes);
-                    ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
-                }
-                if (!__all_sync(0xffffffffu, wait_phase(bar_xready, xparity, p, abort_flag,
-                                                        kStatusSplitTimeout)))
-                    break;
-                if (lane == 0) {
-                    const uint32_t remote_ring = ptx::map_to_cta(sA, partner);
-                    const uint32_t remote_full = ptx::map_to_cta(bar_xfull, partner);
-                    constexpr uint32_t kWarpRows = 32 * kStoreCols * 4;  // this warp's 32 rows of a chunk
-                    for (int c = c_begin; c < c_end; ++c) {
-                        if (c % 2 == j)
-                            continue;
-                        const uint32_t off = uint32_t((c >> 1) * (kRowsPerCta * kStoreCols * 4) +
-                                                      q * 32 * (kStoreCols * 4));
-                        ptx::bulk_copy_to_cluster(remote_ring + off, sB + off, kWarpRows, remote_full);
+                if (lane == 0)
+                    ptx::mbar_arrive(bar_xstaged);
+                if (warp == 2) {
+                    if (!__all_sync(0xffffffffu, wait_phase(bar_xstaged, xparity, p, abort_flag,
+                                                            kStatusSplitTimeout)))
+                        break;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar_xfull, kXchgBytes);
+                        ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
                     }
+                    if (!__all_sync(0xffffffffu, wait_phase(bar_xready, xparity, p, abort_flag,
+                                                            kStatusSplitTimeout)))
+                        break;
+                    if (lane == 0)
+                        ptx::bulk_copy_to_cluster(ptx::map_to_cta(sA, partner), sB, kXchgBytes,
+                                                  ptx::map_to_cta(bar_xfull, partner));
                 }
                 if (!__all_sync(0xffffffffu, wait_phase(bar_xfull, xparity, p, abort_flag,
                                                         kStatusSplitTimeout)))

@@ -105,6 +105,7 @@ class ClockSampler:
         self.device_index = device_index
         self.window = None
         self._t0 = None
+        self.rows = []
 
     def start(self):
         try:
@@ -147,11 +148,18 @@ class ClockSampler:
                              "power_cap": parts[10]})
             except ValueError:
                 continue
+        self.rows = rows
+        return self.summary(self.window)
+
+    def summary(self, window):
+        """Clock / throttle summary of the samples timestamped inside `window`
+        (a (start, end) pair of datetimes; all samples if none fall inside)."""
+        rows = self.rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         in_window = []
-        if self.window:
-            lo, hi = self.window
+        if window:
+            lo, hi = window
             in_window = [r for r in rows if r["t"] is not None and lo <= r["t"] <= hi]
         loaded = in_window or rows
         reasons = set()
@@ -426,22 +434,38 @@ def run_ours(args):
     shapes = {}
     if not args.no_extra:
         def steady(fn, ssets):
-            """Seconds per step: a pilot sizes blocks of about 0.1 s; after a
-            block of warm-up, the median of three timed blocks."""
+            """Seconds per step and the wall-clock window of the timed blocks.
+            Each shape is timed in its own steady state: the GPU first idles for
+            `cooldown` seconds, so that no shape starts from the power-capped
+            clocks of the one before it; then the shape itself runs for about
+            `shape_warmup` seconds, long enough for the clock and power
+            controller to settle on its load (a dense-GEMM loop started after
+            idle first overshoots the power cap and is throttled harder than
+            in its steady state); then the median of three timed blocks of
+            about 0.1 s is taken."""
+            torch.cuda.synchronize()
+            time.sleep(args.cooldown)
             pilot = time_region(fn, ssets, 10, 5, stream) / 1e3 / 10
             it = int(min(5000, max(50, 0.1 / max(pilot, 1e-7))))
-            time_region(fn, ssets, it, 0, stream)
-            return statistics.median(time_region(fn, ssets, it, 0, stream) / 1e3 / it for _ in range(3))
+            for _ in range(max(1, round(args.shape_warmup / 0.1))):
+                time_region(fn, ssets, it, 0, stream)
+            t0 = datetime.datetime.now()
+            per = statistics.median(time_region(fn, ssets, it, 0, stream) / 1e3 / it for _ in range(3))
+            return per, (t0, datetime.datetime.now())
+
+        xsampler = ClockSampler(local_rank)
+        xsampler.start()
+        windows = {}
 
         for name in EXTRA_SHAPES:
             s = SHAPES[name]
             ssets = input_sets(s, device, l2_bytes, max_sets=3)
-            t = steady(ours, ssets)
+            t, windows[name] = steady(ours, ssets)
             if plan.status(stream) != 0:
                 raise SystemExit(f"device status error on {name}")
             cfg = plan.last_config()
             med = statistics.median(time_each(ours, ssets, 50, stream)) / 1e3
-            t_cb = steady(cublas, ssets)
+            t_cb, _ = steady(cublas, ssets)
             r = roofline_entry(s, t, peaks)
             shapes[name] = {"M": s.M, "N": s.N, "K": s.K, "dtype": s.dtype,
                             "us": round(t * 1e6, 2), "median_us": round(med * 1e6, 2),
@@ -453,6 +477,11 @@ def run_ours(args):
                                                                   "split_k", "schedule", "grid")}}
             del ssets
             torch.cuda.empty_cache()
+        xsampler.stop()
+        for name, win in windows.items():
+            c = xsampler.summary(win)
+            shapes[name]["clocks"] = {"sm_mhz": c["sm_mhz"], "reasons": c["reasons"],
+                                      "samples_under_load": c.get("samples_under_load", 0)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -513,6 +542,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cooldown", type=float, default=1.0,
+                    help="idle seconds before each extra shape (ours and cuBLAS alike)")
+    ap.add_argument("--shape-warmup", type=float, default=1.0,
+                    help="seconds each extra shape runs before it is timed")
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for --impl reference")
     args = ap.parse_args(argv)

@@ -150,7 +150,7 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_last_device_status.restype = ctypes.c_uint32
         lib.bwgemm_check_args.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_int]
         lib.bwgemm_check_args.restype = st
-        lib.bwgemm_select_config.argtypes = [i32, i32, i64, i64, i64, ctypes.c_int,
+        lib.bwgemm_select_config.argtypes = [i32, i32, i32, i64, i64, i64, ctypes.c_int,
                                              ctypes.POINTER(PlanOptions), ctypes.POINTER(Config)]
         lib.bwgemm_select_config.restype = st
         lib.bwgemm_plan_last_config.argtypes = [vp, ctypes.POINTER(Config)]
@@ -203,12 +203,13 @@ def _ld(t) -> int:
 
 
 def select_config(num_sms: int, M: int, N: int, K: int, dtype: int = BF16, max_pairs: int = 0,
-                  **opts) -> dict:
+                  max_quads: int = 0, **opts) -> dict:
     """Host-only: the configuration a plan would choose (no GPU needed)."""
     lib = load_library()
     o = make_options(**opts)
     cfg = Config()
-    rc = lib.bwgemm_select_config(num_sms, max_pairs, M, N, K, dtype, ctypes.byref(o), ctypes.byref(cfg))
+    rc = lib.bwgemm_select_config(num_sms, max_pairs, max_quads, M, N, K, dtype, ctypes.byref(o),
+                                  ctypes.byref(cfg))
     if rc != 0:
         raise BwgemmError(rc, "bwgemm_select_config")
     return cfg.as_dict()

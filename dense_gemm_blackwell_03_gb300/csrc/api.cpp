@@ -127,6 +127,44 @@ bwgemm_status_t get_tmap3(TmapSlot& s, const void* ptr, int dtype, int64_t chunk
     return BWGEMM_OK;
 }
 
+// Build (or reuse) the 3-D view of C for paired stores: dimension 0 = 32
+// columns of one chunk, 1 = rows (ldc apart), 2 = whole 32-column chunks (64
+// bytes apart).  A box {32, 32, 2} is two consecutive 64B-swizzled 32 x 32
+// staging buffers.  Only whole chunks are described, so no store reaches past
+// column 32 * chunks.
+bwgemm_status_t get_tmap_cpairs(TmapSlot& s, void* C, int dtype, int64_t rows, int64_t chunks, int64_t ldc)
+{
+    if (s.valid && s.chunks == chunks && s.ptr == C && s.outer == rows && s.ld == ldc && s.dtype == dtype)
+        return BWGEMM_OK;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return BWGEMM_ERR_NO_DEVICE;
+    const cuuint64_t dims[3] = {cuuint64_t(kStoreCols), cuuint64_t(rows), cuuint64_t(chunks)};
+    const cuuint64_t strides[2] = {cuuint64_t(ldc) * 2, cuuint64_t(kStoreCols) * 2};
+    const cuuint32_t box[3] = {uint32_t(kStoreCols), 32, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    s.valid = false;
+    const CUresult r = enc(&s.map,
+                           dtype == BWGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           3, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return BWGEMM_ERR_CUDA;
+    s.ptr = C;
+    s.inner = kStoreCols;
+    s.outer = rows;
+    s.ld = ldc;
+    s.chunks = chunks;
+    s.dtype = dtype;
+    s.box_inner = kStoreCols;
+    s.box_outer = 32;
+    s.swizzle = int(CU_TENSOR_MAP_SWIZZLE_64B);
+    s.valid = true;
+    return BWGEMM_OK;
+}
+
 // Makes the plan's device current for the lifetime of the guard.
 struct DeviceGuard {
     int prev = -1;
@@ -154,7 +192,7 @@ struct bwgemm_plan_s {
     uint32_t* d_status = nullptr;
     uint8_t* d_workspace = nullptr;
     uint64_t workspace_bytes = 0;
-    TmapSlot tmaps[5];  // A, B, C, and the 3-D two-K-block views of A and B
+    TmapSlot tmaps[6];  // A, B, C, the 3-D two-K-block views of A and B, C for paired stores
     bwgemm_config_t last;
     uint64_t launches = 0;
     uint32_t last_status_bits = 0;
@@ -257,10 +295,28 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, c
         p.trace = plan->d_trace;
     }
 
+    // C for stores of two 32-column chunks: a 3-D view of whole chunks with
+    // the operands in order, a 64-row box of the 2-D layout when swapped
+    // (the accumulator's columns are then rows of C)
+    const int64_t c_chunks = N / kStoreCols;
+    bool c_pairs = false;
+    if (sel.swap) {
+        if ((st = get_tmap(plan->tmaps[5], C, dtype, N, M, ldc, kStoreCols, 64, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+            BWGEMM_OK)
+            return st;
+        c_pairs = true;
+    } else if (c_chunks >= 2) {
+        if ((st = get_tmap_cpairs(plan->tmaps[5], C, dtype, M, c_chunks, ldc)) != BWGEMM_OK)
+            return st;
+        c_pairs = true;
+    }
+    p.c_pairs = c_pairs ? 1 : 0;
+    p.c_chunks = int32_t(c_chunks);
+    const CUtensorMap& c2 = c_pairs ? plan->tmaps[5].map : plan->tmaps[2].map;
     const CUtensorMap& a2 = view_a ? plan->tmaps[3].map : plan->tmaps[0].map;
     const CUtensorMap& b2 = view_b ? plan->tmaps[4].map : plan->tmaps[1].map;
     const cudaError_t err = launch_variant(sel.variant_idx, plan->tmaps[0].map, plan->tmaps[1].map,
-                                           plan->tmaps[2].map, a2, b2, p, sel.cfg.grid, stream,
+                                           plan->tmaps[2].map, a2, b2, c2, p, sel.cfg.grid, stream,
                                            opts.pdl_off == 0);
     if (err != cudaSuccess)
         return BWGEMM_ERR_CUDA;

@@ -58,9 +58,11 @@ struct KernelConfig {
     static constexpr int kStageBytes = kABytes + kBBytes;       // per CTA
     static constexpr int kTxBytes = kStageBytes * CG;           // landing per stage on the leader
     static constexpr int kStoreBufBytes = 32 * kStoreCols * 2;  // one 32 x 32 output box
-    static constexpr int kTmemCols = 2 * BN;                    // two fp32 accumulators
-    static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
-                  "TMEM allocation is a power of two in [32, 512] columns");
+    // two fp32 accumulators of BN columns; the allocation is a power of two,
+    // the second accumulator starts half-way (column 256 for BN = 224)
+    static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static constexpr int kAccStride = kTmemCols / 2;
+    static_assert(2 * BN <= kTmemCols && kTmemCols <= 512, "two accumulators fit the TMEM allocation");
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
@@ -448,33 +450,35 @@ __device__ __noinline__ void store_box_ragged(const uint32_t (&packed)[16], cons
     }
 }
 
+// A warp's two staging buffers and the TMA stores reading them.  Single
+// boxes alternate between the buffers; a paired store (two 32-column chunks
+// in one instruction) reads both.
+struct StoreQueue {
+    uint32_t buf;       // shared address of the first 2 KiB buffer
+    int ctr;            // single boxes staged so far
+    bool pair_pending;  // the most recent store read both buffers
+};
+
+// The row end of C lies inside the 32-wide box at box_x and is not on a
+// 16-byte boundary (a TMA store would write past it).
 template <bool TR>
-__device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmParams& p,
-                                          const CUtensorMap* tmap_c, uint32_t my_store,
-                                          int& chunk_ctr, int lane, int col, int m_row)
+__device__ __forceinline__ bool box_is_ragged(const GemmParams& p, int col, int m_row)
 {
-    constexpr int kBufBytes = 32 * kStoreCols * 2;
-    // the row end of C inside this box, not on a 16-byte boundary
     const int row_len = TR ? p.M : p.N;
     const int box_x = TR ? m_row : col;
-    if ((row_len & 7) != 0 && box_x < row_len && box_x + 32 > row_len) {
-        uint32_t packed[16];
+    return (row_len & 7) != 0 && box_x < row_len && box_x + 32 > row_len;
+}
+
+// Convert and write one thread's 32 values into staging buffer sb (64-byte
+// swizzle of the C tensor maps: 16-byte chunk index XOR bits 7-8 of the offset).
+template <bool TR>
+__device__ __forceinline__ void stage_box(const uint32_t (&r)[32], const GemmParams& p, uint32_t sb, int lane)
+{
+    uint32_t packed[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
-        if ((TR ? col : m_row) < (TR ? p.N : p.M))
-            store_box_ragged<TR>(packed, p, lane, col, m_row);
-        return;
-    }
-    const uint32_t sb = my_store + uint32_t((chunk_ctr & 1) * kBufBytes);
+    for (int i = 0; i < 16; ++i)
+        packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
     if constexpr (!TR) {
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
-        if (lane == 0)
-            ptx::bulk_wait_group_read<1>();
-        __syncwarp();
         const uint32_t row_addr = sb + uint32_t(lane * 64);
         const uint32_t swz = uint32_t((lane >> 1) & 3);
 #pragma unroll
@@ -483,13 +487,6 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
                               packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
     } else {
         // box row i = C row (col + i), box column lane = C column (m_row + lane)
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
-        if (lane == 0)
-            ptx::bulk_wait_group_read<1>();
-        __syncwarp();
         const uint32_t in_chunk = uint32_t((lane & 7) * 2);
         const uint32_t chunk = uint32_t(lane >> 3);
 #pragma unroll
@@ -499,6 +496,33 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
             ptx::st_shared_u16(addr, uint16_t(h));
         }
     }
+}
+
+template <bool TR>
+__device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmParams& p,
+                                          const CUtensorMap* tmap_c, StoreQueue& sq, int lane, int col,
+                                          int m_row)
+{
+    constexpr int kBufBytes = 32 * kStoreCols * 2;
+    if (box_is_ragged<TR>(p, col, m_row)) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            packed[i] = pack2(r[2 * i], r[2 * i + 1], p.dtype);
+        if ((TR ? col : m_row) < (TR ? p.N : p.M))
+            store_box_ragged<TR>(packed, p, lane, col, m_row);
+        return;
+    }
+    const uint32_t sb = sq.buf + uint32_t((sq.ctr & 1) * kBufBytes);
+    if (lane == 0) {
+        if (sq.pair_pending)
+            ptx::bulk_wait_group_read<0>();
+        else
+            ptx::bulk_wait_group_read<1>();
+    }
+    sq.pair_pending = false;
+    __syncwarp();
+    stage_box<TR>(r, p, sb, lane);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -510,7 +534,56 @@ __device__ __forceinline__ void store_box(const uint32_t (&r)[32], const GemmPar
         }
         ptx::bulk_commit_group();
     }
-    ++chunk_ctr;
+    ++sq.ctr;
+}
+
+// Two adjacent 32-column chunks (accumulator columns col .. col + 63) as one
+// TMA store: each SM's TMA unit spends about as long on a store as on an
+// operand load, whatever its size, so halving the stores leaves it more time
+// for the loads.  The chunks are staged one after the other into the warp's
+// two buffers (pair_stage), then pair_store issues one store of both: through
+// the 3-D view of C (32 columns x rows x whole 32-column chunks) for the
+// operands in order, through a 64-row box when the accumulator holds C
+// transposed.  Only whole, unragged chunks pair up (pair_ok).
+template <bool TR>
+__device__ __forceinline__ bool pair_ok(const GemmParams& p, int col, int m_row)
+{
+    if (!p.c_pairs || box_is_ragged<TR>(p, col, m_row) || box_is_ragged<TR>(p, col + 32, m_row))
+        return false;
+    return TR || (col / 32 + 1 < p.c_chunks);
+}
+
+__device__ __forceinline__ void pair_begin(StoreQueue& sq, int lane)
+{
+    if (lane == 0)
+        ptx::bulk_wait_group_read<0>();  // no store reads either buffer any more
+    __syncwarp();
+}
+
+template <bool TR>
+__device__ __forceinline__ void pair_stage(const uint32_t (&r)[32], const GemmParams& p, const StoreQueue& sq,
+                                           int half, int lane)
+{
+    stage_box<TR>(r, p, sq.buf + uint32_t(half * 32 * kStoreCols * 2), lane);
+}
+
+template <bool TR>
+__device__ __forceinline__ void pair_store(const GemmParams& p, const CUtensorMap* tmap_c2, StoreQueue& sq,
+                                           int lane, int col, int m_row)
+{
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (m_row < p.M && col < p.N) {
+            if constexpr (!TR)
+                ptx::tma_store_3d(tmap_c2, sq.buf, 0, m_row, col / 32);
+            else
+                ptx::tma_store_2d(tmap_c2, sq.buf, m_row, col);
+        }
+        ptx::bulk_commit_group();
+    }
+    sq.pair_pending = true;
+    sq.ctr = 0;
 }
 
 // MC: CTA pairs per cluster that share each A tile.  Pair i of the cluster
@@ -521,7 +594,8 @@ template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_a2,
-                const __grid_constant__ CUtensorMap tmap_b2, const GemmParams p)
+                const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_c2,
+                const GemmParams p)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
     static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
@@ -529,8 +603,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int CS = CG * MC * KS;  // CTAs per cluster
     // K-slice exchange: each slice sends the other the 32-column chunks it owns,
     // one [128 rows][32 fp32] block per chunk, into the other's idle A ring
-    constexpr int kXchgSlots = BN / kStoreCols / 2;
-    constexpr uint32_t kXchgBytes = uint32_t(kXchgSlots) * kRowsPerCta * kStoreCols * 4;
+    // Ownership of a tile's 32-column chunks by the two K slices of a cluster:
+    // with four or more chunks, pairs of adjacent chunks alternate between the
+    // slices (so each warp stores its own pair with one paired store), else
+    // single chunks do.  The chunks a CTA does not own go to consecutive slots
+    // of its staging block.  With an odd number of chunks (BN = 224) the two
+    // slices own different numbers of them.
+    constexpr int kTileChunks = BN / kStoreCols;
+    constexpr bool kPairOwn = kTileChunks >= 4;
+    constexpr int kXchgSlots = (kTileChunks + 1) / 2;
+    constexpr uint32_t kXchgSlotBytes = uint32_t(kRowsPerCta) * kStoreCols * 4;
+    constexpr uint32_t kXchgBytes = uint32_t(kXchgSlots) * kXchgSlotBytes;
+    auto chunk_owner = [](int c) { return kPairOwn ? ((c >> 1) & 1) : (c & 1); };
+    auto chunk_slot = [](int c) { return kPairOwn ? ((c >> 2) * 2 + (c & 1)) : (c >> 1); };
+    auto owned_chunks = [&](int j) {  // chunks slice j owns
+        int n = 0;
+        for (int c = 0; c < kTileChunks; ++c)
+            n += (chunk_owner(c) == j) ? 1 : 0;
+        return n;
+    };
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kABytes, "exchange fits the A ring");
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kBBytes, "staging fits the B ring");
     extern __shared__ uint8_t smem_raw[];
@@ -588,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_c);
+        if (p.c_pairs)
+            ptx::prefetch_tensormap(&tmap_c2);
         if (p.k_chunks_a > 1)
             ptx::prefetch_tensormap(&tmap_a2);
         if (p.k_chunks_b > 1)
@@ -796,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 ptx::tc_fence_after_sync();
                 trace_unit(p, t - 1, 0);
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg::kAccStride);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(bar_full + 8 * stage, phase, p, abort_flag, kStatusMmaTimeout)) {
                         ok = false;
@@ -841,14 +934,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;
         const int q = warp & 3;
         const int h = ew >> 2;
-        constexpr int kChunks = BN / kStoreCols / 2;  // 32-column chunks per warp
-        const int c_begin = h * kChunks;
-        const int c_end = c_begin + kChunks;
+        // 32-column chunks of a tile: the first half (rounded up) for h = 0
+        constexpr int kHalfChunks = (BN / kStoreCols + 1) / 2;
+        const int c_begin = h * kHalfChunks;
+        const int c_end = h ? BN / kStoreCols : kHalfChunks;
         const int row = q * 32 + lane;
-        const uint32_t my_store = sStore + uint32_t(ew * 2 * Cfg::kStoreBufBytes);
+        StoreQueue sq{sStore + uint32_t(ew * 2 * Cfg::kStoreBufBytes), 0, false};
         constexpr size_t kSlotF4 = size_t(Cfg::kPartialFloats) / 4;  // float4s per CTA partial
         float4* const parts = reinterpret_cast<float4*>(p.partials);
-        int chunk_ctr = 0;
         int t = 0;
         int xchg_count = 0;  // K-slice exchanges done (parity of the exchange barriers)
         Sched iter;
@@ -868,14 +961,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             if (warp == 2 && lane == 0)
                 trace_unit(p, t - 1, 2);
-            const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * BN);
+            const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(buf * Cfg::kAccStride);
             const int cta_row0 = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
             const int m_row = cta_row0 + q * 32;  // first row of this warp's boxes
             const int n_col = w.n_blk * BN;
             if (KS > 1 && w.kind == kUnitSplit) {
                 // ---- split-K inside the cluster: the two K slices of this tile
                 // run on the two pairs (or CTAs) of the cluster.  Chunk c belongs
-                // to slice c % 2.  Each CTA stages the chunks its partner (same
+                // to slice chunk_owner(c).  Each CTA stages the chunks its partner (same
                 // rank in the other slice) owns in its own idle B ring (one
                 // contiguous block); once every epilogue warp has staged its rows,
                 // one thread tells the partner that this CTA's A ring is free and,
@@ -894,14 +987,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++xchg_count;
                 const uint32_t swz = uint32_t(row & 7);
                 auto xoff = [&](int c, int v) -> uint32_t {  // [slot][row][16-byte v ^ row % 8]
-                    return uint32_t((c >> 1) * (kRowsPerCta * kStoreCols * 4) + row * (kStoreCols * 4)) +
+                    return uint32_t(chunk_slot(c) * (kRowsPerCta * kStoreCols * 4) + row * (kStoreCols * 4)) +
                            ((uint32_t(v) ^ swz) << 4);
                 };
                 bool owns_any = false;
                 int last_owned = c_begin;
 #pragma unroll 1
                 for (int c = c_begin; c < c_end; ++c) {
-                    if (c % 2 == j) {
+                    if (chunk_owner(c) == j) {
                         owns_any = true;
                         last_owned = c;
                         continue;
@@ -924,24 +1017,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                             kStatusSplitTimeout)))
                         break;
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar_xfull, kXchgBytes);
+                        // the partner sends the chunks this slice owns
+                        ptx::mbar_arrive_expect_tx(bar_xfull, uint32_t(owned_chunks(j)) * kXchgSlotBytes);
                         ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
                     }
                     if (!__all_sync(0xffffffffu, wait_phase(bar_xready, xparity, p, abort_flag,
                                                             kStatusSplitTimeout)))
                         break;
                     if (lane == 0)
-                        ptx::bulk_copy_to_cluster(ptx::map_to_cta(sA, partner), sB, kXchgBytes,
+                        ptx::bulk_copy_to_cluster(ptx::map_to_cta(sA, partner), sB,
+                                                  uint32_t(owned_chunks(1 - j)) * kXchgSlotBytes,
                                                   ptx::map_to_cta(bar_xfull, partner));
                 }
                 if (!__all_sync(0xffffffffu, wait_phase(bar_xfull, xparity, p, abort_flag,
                                                         kStatusSplitTimeout)))
                     break;
-#pragma unroll 1
-                for (int c = c_begin; c < c_end; ++c) {
-                    if (c % 2 != j)
-                        continue;
-                    uint32_t r[32];
+                // own chunk c: this slice's partial from TMEM + the partner's
+                // from the A ring (two terms: the sum is the same whichever
+                // slice adds)
+                auto sum_chunk = [&](int c, uint32_t (&r)[32]) {
                     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                     uint32_t x[32];
 #pragma unroll
@@ -951,11 +1045,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait();
                     if (c == last_owned)
                         release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
-                    // two terms: the sum is the same whichever slice adds
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(x[i]));
-                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                };
+#pragma unroll 1
+                for (int c = c_begin; c < c_end;) {
+                    if (chunk_owner(c) != j) {
+                        ++c;
+                        continue;
+                    }
+                    const int col = n_col + c * kStoreCols;
+                    uint32_t r[32];
+                    if (c + 1 < c_end && chunk_owner(c + 1) == j && pair_ok<TR>(p, col, m_row)) {
+                        pair_begin(sq, lane);
+                        sum_chunk(c, r);
+                        pair_stage<TR>(r, p, sq, 0, lane);
+                        sum_chunk(c + 1, r);
+                        pair_stage<TR>(r, p, sq, 1, lane);
+                        pair_store<TR>(p, &tmap_c2, sq, lane, col, m_row);
+                        c += 2;
+                    } else {
+                        sum_chunk(c, r);
+                        store_box<TR>(r, p, &tmap_c, sq, lane, col, m_row);
+                        ++c;
+                    }
                 }
                 continue;
             }
@@ -967,15 +1081,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             if (w.kind == kUnitWhole) {
-                // ---- whole tile: TMEM -> registers -> bf16/fp16 -> smem -> TMA store
+                // ---- whole tile: TMEM -> registers -> bf16/fp16 -> smem -> TMA
+                // store, two chunks per store where they pair up
 #pragma unroll 1
-                for (int c = c_begin; c < c_end; ++c) {
+                for (int c = c_begin; c < c_end;) {
+                    const int col = n_col + c * kStoreCols;
                     uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
-                    ptx::tmem_ld_wait();
-                    if (c == c_end - 1)
-                        release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
-                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                    if (c + 1 < c_end && pair_ok<TR>(p, col, m_row)) {
+                        pair_begin(sq, lane);
+                        ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                        ptx::tmem_ld_wait();
+                        pair_stage<TR>(r, p, sq, 0, lane);
+                        ptx::tmem_ld_32x32b_x32(taddr + uint32_t((c + 1) * kStoreCols), r);
+                        ptx::tmem_ld_wait();
+                        if (c + 1 == c_end - 1)
+                            release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
+                        pair_stage<TR>(r, p, sq, 1, lane);
+                        pair_store<TR>(p, &tmap_c2, sq, lane, col, m_row);
+                        c += 2;
+                    } else {
+                        ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
+                        ptx::tmem_ld_wait();
+                        if (c == c_end - 1)
+                            release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
+                        store_box<TR>(r, p, &tmap_c, sq, lane, col, m_row);
+                        ++c;
+                    }
                 }
                 continue;
             }
@@ -1082,7 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             r[4 * v + 2] = __float_as_uint(acc[v].z);
                             r[4 * v + 3] = __float_as_uint(acc[v].w);
                         }
-                        store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                        store_box<TR>(r, p, &tmap_c, sq, lane, n_col + c * kStoreCols, m_row);
                     }
                 }
                 // second arrival: the slice that completes 2S has seen every other
@@ -1189,7 +1320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + sp[v].z);
                         r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + sp[v].w);
                     }
-                    store_box<TR>(r, p, &tmap_c, my_store, chunk_ctr, lane, n_col + c * kStoreCols, m_row);
+                    store_box<TR>(r, p, &tmap_c, sq, lane, n_col + c * kStoreCols, m_row);
                 }
                 __syncwarp();
                 if (lane == 0)

@@ -8,8 +8,8 @@ namespace {
 
 template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                       const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p, int grid,
-                       cudaStream_t stream, bool pdl)
+                       const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
+                       const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     using Cfg = KernelConfig<CG, BN, STAGES>;
     auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
@@ -38,7 +38,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     }
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kernel, a, b, c, a2, b2, p);
+    return cudaLaunchKernelEx(&cfg, kernel, a, b, c, a2, b2, c2, p);
 }
 
 template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
@@ -79,8 +79,8 @@ cudaError_t max_active_one(int* out)
 
 struct VariantFns {
     cudaError_t (*launch)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                          const CUtensorMap&, const CUtensorMap&, const GemmParams&, int, cudaStream_t,
-                          bool);
+                          const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const GemmParams&,
+                          int, cudaStream_t, bool);
     cudaError_t (*max_active)(int*);
     int smem_bytes;
 };
@@ -97,6 +97,7 @@ constexpr VariantFns kFns[] = {
     BWGEMM_VARIANT(1, 128, 6, true, 1, 1),  BWGEMM_VARIANT(1, 64, 8, true, 1, 1),
     BWGEMM_VARIANT(2, 256, 6, false, 2, 1), BWGEMM_VARIANT(2, 128, 8, false, 2, 1),
     BWGEMM_VARIANT(2, 256, 6, false, 1, 2), BWGEMM_VARIANT(1, 64, 8, true, 1, 2),
+    BWGEMM_VARIANT(2, 224, 6, false, 1, 1), BWGEMM_VARIANT(2, 224, 6, false, 1, 2),
 };
 #undef BWGEMM_VARIANT
 static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");
@@ -115,12 +116,12 @@ int find_variant(int cg, int bn, bool trans, int mc, int ks)
 int variant_smem_bytes(int idx) { return (idx >= 0 && idx < kNumVariants) ? kFns[idx].smem_bytes : 0; }
 
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p, int grid,
-                           cudaStream_t stream, bool pdl)
+                           const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
+                           const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
     if (idx < 0 || idx >= kNumVariants)
         return cudaErrorInvalidValue;
-    return kFns[idx].launch(a, b, c, a2, b2, p, grid, stream, pdl);
+    return kFns[idx].launch(a, b, c, a2, b2, c2, p, grid, stream, pdl);
 }
 
 cudaError_t variant_max_active(int idx, int* out)

@@ -18,6 +18,8 @@ namespace bwgemm {
 // clusters of two CTA pairs on adjacent column blocks that multicast their
 // common A tile; the ks = 2 variants run the two K slices of a split-K tile
 // in one cluster and exchange partials through distributed shared memory.
+// The BN = 224 pair variants cut N = 8192 into 37 column tiles, so that one
+// row block (x 2 K slices, or two row blocks) fills 74 of 76 CTA pairs.
 struct Variant {
     int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
     int bn;      // columns of the MMA per unit (= MMA N)
@@ -32,6 +34,7 @@ constexpr Variant kVariants[] = {
     {2, 128, 8, false, 1, 1}, {2, 128, 8, true, 1, 1},  {2, 64, 9, true, 1, 1},
     {1, 128, 6, true, 1, 1},  {1, 64, 8, true, 1, 1},   {2, 256, 6, false, 2, 1},
     {2, 128, 8, false, 2, 1}, {2, 256, 6, false, 1, 2}, {1, 64, 8, true, 1, 2},
+    {2, 224, 6, false, 1, 1}, {2, 224, 6, false, 1, 2},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -44,10 +47,11 @@ int variant_smem_bytes(int idx);
 // Launch variant `idx` with `grid` CTAs (a multiple of its cluster size);
 // with `pdl`, as a programmatic dependent launch (its prologue may overlap the
 // previous kernel on the stream).  a2 / b2: 3-D views of the operands that
-// copy two K blocks at once (used only when p.k_chunks > 1).
+// copy two K blocks at once (used only when p.k_chunks > 1); c2: the view of
+// C that stores two 32-column chunks at once (used only when p.c_pairs).
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const CUtensorMap& a2, const CUtensorMap& b2, const GemmParams& p, int grid,
-                           cudaStream_t stream, bool pdl);
+                           const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
+                           const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
 // Co-resident clusters (of cg * mc CTAs; single CTAs for cg * mc == 1) of
 // variant `idx` on the current device.

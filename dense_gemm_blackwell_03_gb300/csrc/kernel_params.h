@@ -79,6 +79,8 @@ struct GemmParams {
     int32_t pair_copies;    // 1: load two K blocks per copy where the 3-D views allow
     int32_t ks;             // K slices of a tile inside one cluster (1, or 2: split-K whose
                             // two slices exchange partials through distributed shared memory)
+    int32_t c_pairs;        // 1: the second C map stores two 32-column chunks at once
+    int32_t c_chunks;       // whole 32-column chunks of a C row the 3-D C view covers
 };
 
 // Timeline slots of one CTA (nanoseconds of %globaltimer, 0 = not reached).

@@ -188,7 +188,8 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     p.k_chunks_a = p.k_chunks_b = 0;
     p.pair_copies = 0;
     p.prefetch = 0;
-    return launch_variant(sel.variant_idx, ta, tb, tc, ta, tb, p, sel.cfg.grid, s, false) == cudaSuccess
+    // one 32-column chunk per C store (p.c_pairs = 0): no second C view is built
+    return launch_variant(sel.variant_idx, ta, tb, tc, ta, tb, tc, p, sel.cfg.grid, s, false) == cudaSuccess
                ? BWGEMM_OK
                : BWGEMM_ERR_CUDA;
 }

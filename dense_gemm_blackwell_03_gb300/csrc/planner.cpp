@@ -59,7 +59,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     int bn;
     if (opts.tile_n == 0)
         bn = swap ? (Nk <= 64 ? 64 : 128) : (Nk <= 128 ? 128 : 256);
-    else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 256)
+    else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 224 || opts.tile_n == 256)
         bn = opts.tile_n;
     else
         return BWGEMM_ERR_INVALID_ARG;
@@ -76,20 +76,13 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     }
     if (mc > 1 && (cg != 2 || swap))
         return BWGEMM_ERR_UNSUPPORTED;
-    const int idx = find_variant(cg, bn, swap, mc);
-    if (idx < 0)
-        return BWGEMM_ERR_UNSUPPORTED;
     if (opts.split_k < 0 || opts.raster_group < 0 || opts.max_ctas < 0 || opts.prefetch < -1 ||
         opts.prefetch > 64 || opts.copy_kblocks < 0 || opts.copy_kblocks > 2)
         return BWGEMM_ERR_INVALID_ARG;
 
     const int tile_m = kRowsPerCta * cg;
     const int64_t num_m = ceil_div(Mk, tile_m);
-    const int64_t num_n = ceil_div(Nk, int64_t(bn) * mc);  // column groups of mc blocks
     const int64_t num_kb = ceil_div(K, kTileK);
-    const int64_t tiles = num_m * num_n;
-    if (num_m > (1 << 30) || num_n > (1 << 30) || tiles > (int64_t(1) << 30))
-        return BWGEMM_ERR_UNSUPPORTED;
 
     // Workers (clusters of cs CTAs: pairs, pairs of pairs, or single CTAs)
     // the persistent grid holds at once.
@@ -100,6 +93,54 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_CLC)
         return BWGEMM_ERR_INVALID_ARG;
     const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
+
+    // Tile width of the pair form: 224 instead of 256 columns when the
+    // problem fits one wave either way and 224-wide tiles occupy clearly more
+    // of the workers.  N = 8192 makes 32 tiles of 256 (x 2 K slices, or x 2
+    // row blocks: 64 of 76 pairs) but 37 of 224 (74 of 76); a memory-bound
+    // decode shape then streams its weights through 148 SMs instead of 128.
+    // (The occupancy follows the one-wave split rule of the schedule below.)
+    if (opts.tile_n == 0 && cg == 2 && !swap && mc == 1 && bn == 256 && opts.split_k == 0 && !clc &&
+        opts.schedule != BWGEMM_SCHEDULE_STREAM_K) {
+        // tiles, K slices per tile (one-wave rule of the schedule below) and
+        // the share of the workers busy; 0 slices when the launch would take
+        // more than one wave or be left to stream-K
+        struct Wave {
+            int64_t tiles, slices;
+            double occupancy;
+        };
+        auto one_wave = [&](int64_t b) -> Wave {
+            const int64_t t = num_m * ceil_div(Nk, b);
+            if (t == 0 || t > slots)
+                return {t, 0, 0.0};
+            int64_t S = 1;
+            if (num_kb >= 4 && double(t) < 0.8 * double(slots)) {
+                S = std::min<int64_t>({slots / t, num_kb / 4, 4});
+                if (S < 2 || double(t * S) < 0.75 * double(slots))
+                    return {t, 0, 0.0};
+            }
+            return {t, S, double(t * S) / double(slots)};
+        };
+        // Two slices run in one cluster per tile (exchanging partials through
+        // distributed shared memory) only while the tiles fit the co-resident
+        // clusters of four CTAs; trading that exchange for the one through L2
+        // measured slower than the 24 SMs it gains (decode M = 256, N = 8192:
+        // 36 clusters of four fit on GB300, 37 tiles of 224 do not).
+        auto clustered = [&](const Wave& w) {
+            return opts.cluster_split != 1 && w.slices == 2 && w.tiles <= max_quads;
+        };
+        const Wave w256 = one_wave(256), w224 = one_wave(224);
+        if (w256.occupancy > 0.0 && w224.occupancy > w256.occupancy + 0.05 &&
+            !(clustered(w256) && !clustered(w224)))
+            bn = 224;
+    }
+    const int idx = find_variant(cg, bn, swap, mc);
+    if (idx < 0)
+        return BWGEMM_ERR_UNSUPPORTED;
+    const int64_t num_n = ceil_div(Nk, int64_t(bn) * mc);  // column groups of mc blocks
+    const int64_t tiles = num_m * num_n;
+    if (num_m > (1 << 30) || num_n > (1 << 30) || tiles > (int64_t(1) << 30))
+        return BWGEMM_ERR_UNSUPPORTED;
     if (clc && opts.split_k > 1)
         return BWGEMM_ERR_INVALID_ARG;  // cluster launch control hands out whole tiles only
 
@@ -327,8 +368,8 @@ bwgemm_status_t bwgemm_check_args(const void* A, const void* B, const void* C, i
     return BWGEMM_OK;
 }
 
-bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
-                                     int64_t K, bwgemm_dtype_t dtype,
+bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int32_t max_quads,
+                                     int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype,
                                      const bwgemm_plan_options_t* opts, bwgemm_config_t* out)
 {
     if (!out || (dtype != BWGEMM_BF16 && dtype != BWGEMM_FP16))
@@ -340,7 +381,7 @@ bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t
         bwgemm_default_options(&o);
     const uint64_t ws = o.workspace_bytes ? o.workspace_bytes : (64ull << 20);
     Selection sel;
-    const bwgemm_status_t st = select_config(num_sms, max_pairs, 0, M, N, K, o, ws, &sel);
+    const bwgemm_status_t st = select_config(num_sms, max_pairs, max_quads, M, N, K, o, ws, &sel);
     if (st == BWGEMM_OK)
         *out = sel.cfg;
     return st;

@@ -99,10 +99,16 @@ def main(argv=None) -> int:
     ap.add_argument("--schedule", type=int, default=0)
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--warmup", type=int, default=6)
+    ap.add_argument("--opt", action="append", default=[], metavar="NAME=INT",
+                    help="any other plan option (repeatable), e.g. --opt multicast=2")
     args = ap.parse_args(argv)
+    opts = {}
+    for kv in args.opt:
+        name, _, value = kv.partition("=")
+        opts[name] = int(value)
     s = SHAPES[args.shape]
     sets = [make_inputs(s, device="cuda", seed=100 + i) for i in range(3)]
-    with binding.Plan(0, trace=1, schedule=args.schedule, split_k=args.split_k) as plan:
+    with binding.Plan(0, trace=1, schedule=args.schedule, split_k=args.split_k, **opts) as plan:
         for i in range(args.warmup):
             plan.gemm(*sets[i % 3])
         torch.cuda.synchronize()

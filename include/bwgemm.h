@@ -78,7 +78,9 @@ typedef enum {
  * defaults with bwgemm_default_options(). */
 typedef struct {
     int32_t variant;          /* bwgemm_variant_t                                       */
-    int32_t tile_n;           /* 0 = auto, 64, 128 or 256: MMA N per work unit          */
+    int32_t tile_n;           /* 0 = auto, 64, 128, 224 or 256: MMA N per work unit
+                                 (224: CTA-pair form, operands not swapped, no
+                                 multicast)                                             */
     int32_t split_k;          /* 0 = auto, 1 = off, s >= 2: s K-slices per tile         */
     int32_t raster_group;     /* 0 = auto; m-blocks walked before stepping along N      */
     int32_t max_ctas;         /* 0 = fill the GPU; else cap on the persistent grid      */
@@ -213,11 +215,12 @@ bwgemm_status_t bwgemm_check_args(const void* A, const void* B, const void* C, i
 /*
  * Host-only: the configuration a plan with `opts` (NULL = defaults) would
  * pick for this shape on a GPU with `num_sms` SMs that can hold
- * `max_pairs` co-resident CTA pairs (0 = num_sms / 2) and max_pairs / 2
- * co-resident clusters of two pairs (the multicast form).  No device access.
+ * `max_pairs` co-resident CTA pairs (0 = num_sms / 2) and `max_quads`
+ * co-resident clusters of two pairs (0 = max_pairs / 2; the multicast form
+ * and the clustered split-K).  No device access.
  */
-bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
-                                     int64_t K, bwgemm_dtype_t dtype,
+bwgemm_status_t bwgemm_select_config(int32_t num_sms, int32_t max_pairs, int32_t max_quads,
+                                     int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype,
                                      const bwgemm_plan_options_t* opts, bwgemm_config_t* out);
 
 /* The configuration of the plan's most recent bwgemm_run / bwgemm_run_host. */

@@ -102,8 +102,8 @@ def test_check_args(lib, args, want):
     assert binding.check_args(*args) == want
 
 
-def cfg(M, N, K, sms=148, pairs=0, **opts):
-    return binding.select_config(sms, M, N, K, max_pairs=pairs, **opts)
+def cfg(M, N, K, sms=148, pairs=0, quads=0, **opts):
+    return binding.select_config(sms, M, N, K, max_pairs=pairs, max_quads=quads, **opts)
 
 
 def test_select_square_uses_cta_pairs_and_stream_k():
@@ -139,20 +139,40 @@ def test_select_small_m_splits_k_in_one_wave():
 
 
 def test_select_decode_shapes():
-    # attention out / MLP down: 32 tiles of 256 x 256 over 76 pairs -> 2 slices each
+    # attention out / MLP down on GB300 (76 pairs, 36 clusters of four): 32
+    # tiles of 256 x 2 K slices, each tile's slices in one cluster.  224-wide
+    # tiles (37 x 2 = 74 pairs) would need 37 clusters: their slices would
+    # reduce through L2, which measured slower -> 256
     for N, K in ((8192, 8192), (8192, 28672)):
-        c = cfg(256, N, K, sms=152, pairs=76, swap_ab=1)
-        assert c["variant"] == 2 and c["num_tiles"] == 32 and c["split_k"] == 2
-        assert c["split_scatter"] == 1 and c["grid"] == 128
+        c = cfg(256, N, K, sms=152, pairs=76, quads=36, swap_ab=1)
+        assert c["variant"] == 2 and c["tile_n"] == 256 and c["num_tiles"] == 32
+        assert c["split_k"] == 2 and c["cluster_split"] == 1 and c["grid"] == 128
+        # with room for 37 clusters of four the 224-wide tiles keep the cluster
+        c = cfg(256, N, K, sms=152, pairs=76, quads=38, swap_ab=1)
+        assert c["tile_n"] == 224 and c["num_tiles"] == 37 and c["cluster_split"] == 1
+        assert c["grid"] == 148
     # fused QKV: 40 tiles, 2 slices would not fit one wave -> stream-K over all pairs
     c = cfg(256, 10240, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
     # MLP up: 112 tiles = 1.47 waves -> stream-K
     c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["dp_tiles"] == 0
-    # Gemma-like 512 x 8192 x 5376: 64 tiles fill 84 % of the pairs -> whole tiles
+    # Gemma-like 512 x 8192 x 5376: 2 x 37 tiles of 224 fill 74 of 76 pairs
+    # (2 x 32 of 256 would fill 64) -> whole tiles of 224
     c = cfg(512, 8192, 5376, sms=152, pairs=76)
-    assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 128
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 148
+    assert c["tile_n"] == 224 and c["num_tiles"] == 74
+    # the 224-wide rule stays out of multi-wave, stream-K, forced and 1-SM cases
+    assert cfg(4096, 4096, 4096, sms=152, pairs=76)["tile_n"] == 256
+    assert cfg(256, 10240, 8192, sms=152, pairs=76)["tile_n"] == 256
+    assert cfg(256, 8192, 8192, sms=152, pairs=76, split_k=2)["tile_n"] == 256
+    assert cfg(256, 8192, 8192, sms=152, pairs=76, multicast=2)["tile_n"] == 256
+    assert cfg(128, 8192, 8192, sms=152, pairs=76)["tile_n"] == 256
+    # explicit 224 exists only in the pair form with the operands in order
+    assert cfg(1000, 2000, 512, tile_n=224, variant=2)["tile_n"] == 224
+    for bad in (dict(variant=1), dict(swap_ab=2), dict(multicast=2)):
+        with pytest.raises(binding.BwgemmError):
+            cfg(1000, 2000, 512, tile_n=224, **bad)
 
 
 def test_select_swapped_operands_for_small_m():
@@ -219,9 +239,11 @@ def test_select_multicast_pairs_of_pairs():
 
 def test_select_cluster_split():
     # one-wave split-K with two slices: the slices of a tile share a cluster
-    c = cfg(256, 8192, 8192, sms=152, pairs=76)
+    c = cfg(256, 8192, 8192, sms=152, pairs=76, tile_n=256)
     assert c["cluster_split"] == 1 and c["split_k"] == 2 and c["grid"] == 32 * 4
     assert c["workspace_bytes"] == 0
+    c = cfg(256, 8192, 8192, sms=152, pairs=76)  # 37 tiles of 224 (38 clusters of four fit)
+    assert c["tile_n"] == 224 and c["cluster_split"] == 1 and c["grid"] == 37 * 4
     c = cfg(16, 8192, 8192, sms=152, pairs=76)  # swapped: clusters of two single CTAs
     assert c["swap_ab"] == 1 and c["cluster_split"] == 1 and c["grid"] == 64 * 2
     c = cfg(256, 8192, 8192, sms=152, pairs=76, cluster_split=1)
@@ -259,7 +281,7 @@ def test_select_kblocks_per_copy():
 
 def test_select_tiles_schedule_splits_k():
     c = cfg(256, 8192, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_TILES, swap_ab=1,
-            cluster_split=1)
+            cluster_split=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 2
     assert c["num_units"] == 64 and c["grid"] == 128 and c["split_scatter"] == 1
     assert c["workspace_bytes"] == (1 << 20) + 32 * 2 * 2 * 128 * 256 * 4  # partials through L2

@@ -88,7 +88,7 @@ def test_strided_operands_and_output(plan):
     assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
 
 
-@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 224), (2, 256)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_every_variant(variant, tile_n, dtype):
     A = make_matrix(520, 640, "normal", dtype, seed=800, device="cuda")
@@ -267,6 +267,46 @@ def test_tune_rejects_bad_arguments():
         C = torch.empty((64, 60), dtype=torch.bfloat16, device="cuda")
         with pytest.raises(binding.BwgemmError):
             p.tune(A, A[:60].contiguous(), out=C[:, :60], iters=1)  # ldc 60: misaligned
+
+
+# ------------------------------------------- 224-column tiles of the pair form
+@pytest.mark.parametrize("M,N,K", [(256, 2048, 1024), (200, 1000, 1000), (500, 3000, 640),
+                                   (40, 1800, 1088)])
+@pytest.mark.parametrize("opts", [
+    dict(schedule=binding.SCHEDULE_TILES),                                  # whole tiles
+    dict(schedule=binding.SCHEDULE_TILES, copy_kblocks=2),
+    dict(split_k=2, cluster_split=1, schedule=binding.SCHEDULE_TILES),      # slices through L2
+    dict(split_k=2, cluster_split=2, schedule=binding.SCHEDULE_TILES),      # slices in one cluster
+    dict(split_k=3, schedule=binding.SCHEDULE_TILES),
+    dict(schedule=binding.SCHEDULE_STREAM_K, max_ctas=24),
+    dict(schedule=binding.SCHEDULE_CLC),
+])
+def test_tile224_exact(M, N, K, opts):
+    # 7 store chunks of 32 columns per tile (an odd count: the two K slices of
+    # a cluster own 4 and 3 of them), the second accumulator at TMEM column
+    # 256, ragged M, N and K; integer inputs, run twice
+    A = make_matrix(M, K, "int2", seed=3700 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=3710 + N, device="cuda")
+    with binding.Plan(0, variant=2, tile_n=224, swap_ab=1, **opts) as p:
+        for _ in range(2):
+            run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["tile_n"] == 224 and c["variant"] == 2
+        if opts.get("cluster_split") == 2:
+            assert c["cluster_split"] == 1
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tile224_auto_two_row_blocks(dtype):
+    # the planner's choice for two row blocks over N = 8192 (2 x 37 whole
+    # tiles of 224 on 74 of 76 pairs) on N(0,1) activations and N(0, 0.02^2)
+    # weights
+    A = make_matrix(512, 512, "normal", dtype, seed=3720, device="cuda")
+    B = make_matrix(8192, 512, "weight", dtype, seed=3721, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, dtype)
+        c = p.last_config()
+        assert c["tile_n"] == 224 and c["num_tiles"] == 74 and c["split_k"] == 1
 
 
 # ------------------------------ split-K slices exchanging in distributed shared memory

@@ -1,0 +1,173 @@
+"""Ablations of the design steps both pages walk through, on GB300.
+
+``python -m dense_gemm_blackwell_03_gb300.ablations [--shape NAME ...]``
+times one launch configuration per row of ``ABLATIONS`` on each named
+workload and prints one JSON line per (shape, row): TFLOP/s, GB/s, the
+fraction of the roofline ``min(peak, AI x BW)`` and the change against the
+default plan.  Each row switches one plan option against the default, so it
+measures what that step of the design is worth here:
+
+- CTA pairs (``cta_group::2``, 256-row units) against one CTA per 128-row unit:
+  "Matrix Multiplication on NVIDIA's Blackwell", Kernel 5; "Writing a
+  Blackwell GEMM by hand", the 2-CTA step.
+- Tile width (MMA N 128 / 224 / 256).
+- One or two K blocks per TMA copy (a design choice of this library: a copy
+  costs the SM's TMA unit about the same time whatever its size).
+- Schedules: whole tiles in grouped raster order, stream-K, cluster launch
+  control (deep dive Kernel 8), and grouped raster against plain row order
+  (deep dive Kernel 9).
+- A multicast across two CTA pairs (deep dive Kernel 5's 2x2 cluster; the
+  CuTeDSL post's multicast step).
+- Split-K: slices in one cluster exchanging through distributed shared
+  memory against slices reducing through L2.
+- Operand order for small M (C^T = B A^T).
+
+Steps fixed at compile time (128B swizzle, the ring depth, the TMEM
+double buffer) have no switch and are not timed here.  Timing: each row runs
+about ``--warmup`` seconds, then the median of three blocks of about 0.1 s
+is taken, with CUDA events on the launching stream; inputs rotate over
+copies larger than L2.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+import time
+
+# (label, plan options, what the row isolates)
+ABLATIONS = [
+    ("default", {}, "the planner's choice"),
+    ("one CTA per unit", {"variant": 1}, "CTA pairs (cta_group::2) off"),
+    ("CTA pair", {"variant": 2}, "CTA pairs forced"),
+    ("tile N 128", {"tile_n": 128}, "narrower MMA N"),
+    ("tile N 224", {"tile_n": 224, "variant": 2, "swap_ab": 1}, "224-column pair tiles"),
+    ("tile N 256", {"tile_n": 256}, "256-column tiles"),
+    ("1 K block per copy", {"copy_kblocks": 1}, "one TMA copy per K block and operand"),
+    ("2 K blocks per copy", {"copy_kblocks": 2}, "one TMA copy per two K blocks"),
+    ("whole tiles", {"schedule": 1}, "static persistent schedule, no stream-K"),
+    ("stream-K", {"schedule": 2}, "stream-K over the last wave"),
+    ("cluster launch control", {"schedule": 3}, "clusters cancel pending launches"),
+    ("raster group 1", {"raster_group": 1}, "row-order tiles instead of groups of 8"),
+    ("A multicast", {"multicast": 2}, "two pairs share each A tile"),
+    ("split-K through L2", {"cluster_split": 1}, "clustered split-K exchange off"),
+    ("operands in order", {"swap_ab": 1}, "C^T = B A^T off"),
+]
+
+DEFAULT_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out", "tail_m64"]
+
+
+def _steady(run, sets, warmup_s):
+    """Seconds per launch in steady state (CUDA events, median of 3 blocks)."""
+    import torch
+    stream = torch.cuda.current_stream()
+
+    def block(n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            run(*sets[i % len(sets)])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    pilot = block(10) / 10
+    n = int(min(5000, max(20, 0.1 / max(pilot, 1e-7))))
+    t_end = time.perf_counter() + warmup_s
+    while time.perf_counter() < t_end:
+        block(n)
+    return statistics.median(block(n) / n for _ in range(3))
+
+
+def _peaks():
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def _input_sets(shape, l2_bytes):
+    import math
+
+    import torch
+
+    from .workloads import TORCH_DTYPES, make_inputs
+    n = 1 if shape.algorithmic_bytes >= 2 * l2_bytes else min(3, math.ceil(3 * l2_bytes / shape.algorithmic_bytes))
+    sets = []
+    for i in range(n):
+        A, B = make_inputs(shape, device="cuda", seed=None if i == 0 else 7919 * i + 17)
+        C = torch.empty((shape.M, shape.N), dtype=TORCH_DTYPES[shape.dtype], device="cuda")
+        sets.append((A, B, C))
+    return sets
+
+
+def main(argv=None) -> int:
+    import torch
+
+    from . import binding
+    from .workloads import SHAPES
+
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--shape", action="append", choices=sorted(SHAPES),
+                    help="workload (repeatable; default: 4096^3, prefill attention-out, "
+                         "decode attention-out, M = 64 tail)")
+    ap.add_argument("--warmup", type=float, default=0.3, help="seconds of each row's own load before timing")
+    ap.add_argument("--cooldown", type=float, default=0.5, help="idle seconds before each row")
+    args = ap.parse_args(argv)
+    binding.load_library(build_if_missing=True)
+    hbm_gbs, tflops_peak, peak_src = _peaks()
+    props = torch.cuda.get_device_properties(0)
+    l2_bytes = int(getattr(props, "L2_cache_size", 129 * 10 ** 6)) or 129 * 10 ** 6
+    for name in args.shape or DEFAULT_SHAPES:
+        s = SHAPES[name]
+        sets = _input_sets(s, l2_bytes)
+        ai = s.flops / s.algorithmic_bytes
+        attainable = min(tflops_peak, ai * hbm_gbs / 1e3)
+        base_t = None
+        base_cfg = None
+        for label, opts, what in ABLATIONS:
+            row = {"shape": name, "row": label, "options": opts, "isolates": what}
+            try:
+                plan = binding.Plan(0, **opts)
+                plan.gemm(*sets[0][:2], out=sets[0][2])
+            except binding.BwgemmError as e:
+                row["result"] = f"not applicable: {e}"
+                print(json.dumps(row), flush=True)
+                continue
+            cfg = plan.last_config()
+            if base_cfg is not None and cfg == base_cfg:
+                row["result"] = "same configuration as the default"
+                print(json.dumps(row), flush=True)
+                plan.close()
+                continue
+            torch.cuda.synchronize()
+            time.sleep(args.cooldown)
+            t = _steady(lambda A, B, C: plan.gemm(A, B, out=C), sets, args.warmup)
+            status = plan.status()
+            plan.close()
+            if status != 0:
+                raise SystemExit(f"device status {status} on {name} / {label}")
+            tflops = s.flops / t / 1e12
+            row.update({"us": round(t * 1e6, 2), "tflops": round(tflops, 1),
+                        "gbs": round(s.algorithmic_bytes / t / 1e9, 1),
+                        "roofline_frac": round(tflops / attainable, 4), "peak_source": peak_src,
+                        "config": {k: cfg[k] for k in ("variant", "tile_n", "split_k", "schedule", "grid",
+                                                       "copy_kblocks", "multicast", "cluster_split",
+                                                       "swap_ab", "raster_group")}})
+            if base_t is None:
+                base_t, base_cfg = t, cfg
+            else:
+                row["vs_default"] = round(base_t / t, 4)
+            print(json.dumps(row), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

@@ -124,6 +124,17 @@ __device__ __forceinline__ void raster(const GemmParams& p, int tile, int& m_blk
     n_blk = local / gm;
 }
 
+// First K block of slice i of S over kb K blocks, floor(i * kb / S): in 32-bit
+// arithmetic when the product fits (a 64-bit division is a long subroutine,
+// and the MMA thread works out each unit's range between two units, while the
+// tensor pipe drains).
+__device__ __forceinline__ int slice_begin(int i, int kb, int S)
+{
+    if ((long long)i * kb < (1ll << 31))
+        return int(unsigned(i) * unsigned(kb) / unsigned(S));
+    return int((long long)i * kb / S);
+}
+
 // First stream-K iteration of `worker` (of `workers`).
 __device__ __forceinline__ long long sk_begin(const GemmParams& p, int worker, int workers)
 {
@@ -155,7 +166,7 @@ struct UnitIter {
     {
         if (it < it_end) {
             const int KB = p.num_k_blocks;
-            const int t = int(it / KB);
+            const int t = (it < (1ll << 31)) ? int(unsigned(it) / unsigned(KB)) : int(it / KB);
             w.kb0 = int(it - (long long)t * KB);
             w.kb1 = int(min((long long)KB, (long long)w.kb0 + (it_end - it)));
             w.kind = (w.kb0 == 0 && w.kb1 == KB) ? kUnitWhole : kUnitStreamK;
@@ -171,8 +182,8 @@ struct UnitIter {
             const int S = p.split_k;
             w.tile = u / S;
             w.split = S - 1 - (u - w.tile * S);
-            w.kb0 = int((long long)w.split * p.num_k_blocks / S);
-            w.kb1 = int((long long)(w.split + 1) * p.num_k_blocks / S);
+            w.kb0 = slice_begin(w.split, p.num_k_blocks, S);
+            w.kb1 = slice_begin(w.split + 1, p.num_k_blocks, S);
             w.kind = (S > 1) ? kUnitSplit : kUnitWhole;
             w.sk_tile = 0;
             w.slot = 0;
@@ -267,8 +278,8 @@ struct Sched {
             if (ks > 1) {
                 // the cluster's pairs take the K slices of one tile, in K order
                 w.split = pair;
-                w.kb0 = int((long long)pair * p.num_k_blocks / ks);
-                w.kb1 = int((long long)(pair + 1) * p.num_k_blocks / ks);
+                w.kb0 = slice_begin(pair, p.num_k_blocks, ks);
+                w.kb1 = slice_begin(pair + 1, p.num_k_blocks, ks);
                 w.kind = kUnitSplit;
             } else {
                 w.n_blk = w.n_blk * mc + pair;

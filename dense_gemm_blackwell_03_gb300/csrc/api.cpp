@@ -199,6 +199,11 @@ struct bwgemm_plan_s {
     // device staging buffers of bwgemm_run_host
     void* h2d[3] = {nullptr, nullptr, nullptr};
     size_t h2d_cap[3] = {0, 0, 0};
+    // bwgemm_run_host's pipeline over row blocks: copy-in, GEMM and copy-out
+    // streams and their events (created on first use)
+    cudaStream_t side[3] = {nullptr, nullptr, nullptr};
+    cudaEvent_t events[2 * kHostChunksMax + 2] = {};
+    bool side_ready = false;
     // optional timeline (opts.trace): kTraceSlots stamps per CTA of the last launch
     uint64_t* d_trace = nullptr;
     int trace_ctas = 0;
@@ -426,6 +431,12 @@ bwgemm_status_t bwgemm_destroy(bwgemm_plan_t plan)
     cudaFree(plan->d_workspace);
     if (plan->d_trace)
         cudaFree(plan->d_trace);
+    for (cudaStream_t x : plan->side)
+        if (x)
+            cudaStreamDestroy(x);
+    for (cudaEvent_t e : plan->events)
+        if (e)
+            cudaEventDestroy(e);
     for (void* b : plan->h2d)
         if (b)
             cudaFree(b);
@@ -500,22 +511,72 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
         return st;
     // one linear copy when the host rows are already packed like the device copy
     auto copy_rows = [&](void* dst, int64_t dld, const void* src, int64_t sld, int64_t cols,
-                         int64_t rows, cudaMemcpyKind kind) {
+                         int64_t rows, cudaMemcpyKind kind, cudaStream_t cs) {
         if (sld == dld && dld == cols)
-            return cudaMemcpyAsync(dst, src, size_t(rows) * size_t(cols) * 2, kind, s);
+            return cudaMemcpyAsync(dst, src, size_t(rows) * size_t(cols) * 2, kind, cs);
         return cudaMemcpy2DAsync(dst, size_t(dld) * 2, src, size_t(sld) * 2, size_t(cols) * 2,
-                                 size_t(rows), kind, s);
+                                 size_t(rows), kind, cs);
     };
+    const bwgemm_plan_options_t& opts = options_for(plan, M, N, K, dtype);
+    const int64_t rows = host_block_rows(M, N, K);
+    const int chunks = rows > 0 ? int((M + rows - 1) / rows) : 1;
+    if (chunks > 1) {
+        // Pipeline over row blocks of A and C: B goes over first, then row
+        // block i of A on the copy-in stream, its GEMM on the compute stream,
+        // and its rows of C back on the copy-out stream, so that the GEMMs and
+        // the copies of C overlap the copies of A (the link to host memory,
+        // not the GPU, bounds a call of this size).
+        if (!plan->side_ready) {
+            for (cudaStream_t& x : plan->side)
+                if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess)
+                    return BWGEMM_ERR_CUDA;
+            for (cudaEvent_t& e : plan->events)
+                if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                    return BWGEMM_ERR_CUDA;
+            plan->side_ready = true;
+        }
+        cudaStream_t s_in = plan->side[0], s_mm = plan->side[1], s_out = plan->side[2];
+        cudaEvent_t ev_start = plan->events[2 * kHostChunksMax];
+        cudaEvent_t ev_end = plan->events[2 * kHostChunksMax + 1];
+        if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_mm, ev_start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess ||
+            copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice, s_in) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+        uint8_t* dA = static_cast<uint8_t*>(plan->h2d[0]);
+        uint8_t* dC = static_cast<uint8_t*>(plan->h2d[2]);
+        for (int i = 0; i < chunks; ++i) {
+            const int64_t r0 = i * rows, r = std::min<int64_t>(rows, M - r0);
+            if (r <= 0)
+                break;
+            cudaEvent_t ev_in = plan->events[2 * i], ev_mm = plan->events[2 * i + 1];
+            const uint8_t* hA = static_cast<const uint8_t*>(A_host) + size_t(r0) * size_t(lda) * 2;
+            uint8_t* hC = static_cast<uint8_t*>(C_host) + size_t(r0) * size_t(ldc) * 2;
+            if (copy_rows(dA + size_t(r0) * dlda * 2, dlda, hA, lda, K, r, cudaMemcpyHostToDevice, s_in) !=
+                    cudaSuccess ||
+                cudaEventRecord(ev_in, s_in) != cudaSuccess || cudaStreamWaitEvent(s_mm, ev_in, 0) != cudaSuccess)
+                return BWGEMM_ERR_CUDA;
+            if ((st = enqueue(plan, opts, dA + size_t(r0) * dlda * 2, plan->h2d[1], dC + size_t(r0) * dldc * 2, r,
+                              N, K, dlda, dlda, dldc, dtype, s_mm)) != BWGEMM_OK)
+                return st;
+            if (cudaEventRecord(ev_mm, s_mm) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_mm, 0) != cudaSuccess ||
+                copy_rows(hC, ldc, dC + size_t(r0) * dldc * 2, dldc, N, r, cudaMemcpyDeviceToHost, s_out) !=
+                    cudaSuccess)
+                return BWGEMM_ERR_CUDA;
+        }
+        if (cudaEventRecord(ev_end, s_out) != cudaSuccess || cudaStreamWaitEvent(s, ev_end, 0) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+        return bwgemm_get_status(plan, stream);
+    }
     if (K > 0) {
-        if (copy_rows(plan->h2d[0], dlda, A_host, lda, K, M, cudaMemcpyHostToDevice) != cudaSuccess ||
-            copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice) != cudaSuccess)
+        if (copy_rows(plan->h2d[0], dlda, A_host, lda, K, M, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return BWGEMM_ERR_CUDA;
     }
-    st = enqueue(plan, options_for(plan, M, N, K, dtype), plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N,
-                 K, dlda, dlda, dldc, dtype, s);
+    st = enqueue(plan, opts, plan->h2d[0], plan->h2d[1], plan->h2d[2], M, N, K, dlda, dlda, dldc, dtype, s);
     if (st != BWGEMM_OK)
         return st;
-    if (copy_rows(C_host, ldc, plan->h2d[2], dldc, N, M, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (copy_rows(C_host, ldc, plan->h2d[2], dldc, N, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return BWGEMM_ERR_CUDA;
     return bwgemm_get_status(plan, stream);
 }

@@ -57,6 +57,13 @@ cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, 
 // variant `idx` on the current device.
 cudaError_t variant_max_active(int idx, int* out);
 
+// bwgemm_run_host: rows of A and C per block of its copy/compute pipeline
+// (0: one block, no pipeline).  Blocks are whole 256-row tiles, at least 512
+// rows, at most kHostChunksMax of them, and only calls that move >= 16 MiB
+// are split (below that the copies are too short to hide a GEMM behind).
+constexpr int kHostChunksMax = 8;
+int64_t host_block_rows(int64_t M, int64_t N, int64_t K);
+
 // Sizes of the split-K workspace regions.
 constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) arrival counters
 

@@ -290,6 +290,16 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     return BWGEMM_OK;
 }
 
+int64_t host_block_rows(int64_t M, int64_t N, int64_t K)
+{
+    const int64_t bytes = 2 * (M * K + N * K + M * N);
+    if (K <= 0 || N <= 0 || M < 1024 || bytes < (int64_t(16) << 20))
+        return 0;
+    const int64_t blocks = std::min<int64_t>(kHostChunksMax, M / 512);
+    const int64_t rows = ceil_div(ceil_div(M, blocks), 256) * 256;
+    return rows < M ? rows : 0;
+}
+
 GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype)
 {
     const Variant& v = kVariants[sel.variant_idx];

@@ -491,6 +491,26 @@ def test_host_buffers_round_trip(plan):
     compare(bits_of(C), ref, "bf16", 264, exact=True)
 
 
+@pytest.mark.parametrize("M,lda_pad,ldc_pad", [(2000, 0, 0), (1536, 8, 16), (1100, 24, 0)])
+def test_host_buffers_pipelined(M, lda_pad, ldc_pad):
+    # calls moving >= 16 MiB run as a pipeline over row blocks (A in, GEMM, C
+    # out on three streams); ragged last block, host strides wider than the
+    # rows, run twice on one plan
+    K, N = 2048, 2048
+    Abuf = make_matrix(M, K + lda_pad, "int2", seed=940 + M).pin_memory()
+    A = Abuf[:, :K]
+    B = make_matrix(N, K, "int2", seed=941).pin_memory()
+    Cbuf = torch.full((M, N + ldc_pad), 5.0, dtype=torch.bfloat16).pin_memory()
+    C = Cbuf[:, :N]
+    ref = oracle.gemm(bits_of(A.contiguous()), bits_of(B), "bf16")
+    with binding.Plan(0) as p:
+        for _ in range(2):
+            p.gemm_host(A, B, out=C)
+            compare(bits_of(C.contiguous()), ref, "bf16", K, exact=True)
+    if ldc_pad:
+        assert torch.all(Cbuf[:, N:] == 5.0)
+
+
 # ------------------------------------------------------- the pages' full shapes
 FULL = ["square4096", "square4096_fp16", "prefill_attn_out", "prefill_mlp_up",
         "decode_attn_out", "decode_qkv", "decode_mlp_up", "decode_mlp_down",

@@ -50,7 +50,13 @@ namespace bwgemm {
 template <int CG, int BN, int STAGES>
 struct KernelConfig {
     static_assert(CG == 1 || CG == 2, "CTA group is 1 or 2");
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN in [64, 256], multiple of 32");
+    static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || (CG == 2 && BN == 320)),
+                  "BN in [64, 256] (multiple of 32), or 320 for the CTA pair");
+    // columns of the first and second MMA of a K step: one MMA up to 256
+    // columns; a 320-column unit issues N = 256 and N = 64 into one 320-column
+    // accumulator, the second reading the last 32 B rows of each CTA's stage
+    static constexpr int kMmaN1 = BN <= 256 ? BN : 256;
+    static constexpr int kMmaN2 = BN - kMmaN1;
     static constexpr int kTileM = CG * kRowsPerCta;             // rows per work unit
     static constexpr int kBRows = (CG == 1) ? BN : BN / 2;      // B rows this CTA loads
     static constexpr int kABytes = kRowsPerCta * kTileK * 2;    // 16 KiB
@@ -60,9 +66,11 @@ struct KernelConfig {
     static constexpr int kStoreBufBytes = 32 * kStoreCols * 2;  // one 32 x 32 output box
     // two fp32 accumulators of BN columns; the allocation is a power of two,
     // the second accumulator starts half-way (column 256 for BN = 224)
-    static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    // (two when both fit the 512 TMEM columns, else one: a 320-column unit)
+    static constexpr int kAccBufs = (2 * BN <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = (kAccBufs * BN <= 128) ? 128 : (kAccBufs * BN <= 256) ? 256 : 512;
     static constexpr int kAccStride = kTmemCols / 2;
-    static_assert(2 * BN <= kTmemCols && kTmemCols <= 512, "two accumulators fit the TMEM allocation");
+    static_assert(kAccBufs * BN <= kTmemCols && kTmemCols <= 512, "the accumulators fit the TMEM allocation");
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
@@ -82,6 +90,21 @@ struct KernelConfig {
     // floats of one CTA's fp32 partial tile
     static constexpr int kPartialFloats = kRowsPerCta * BN;
 };
+
+// Column of the tile (relative to its first column) that accumulator chunk c
+// (32 columns) holds.  Up to 256 columns the accumulator is the tile.  In a
+// 320-column unit each CTA of the pair stages B rows [0, 160) of its half;
+// the first MMA (N = 256) reads rows [0, 128) of both halves (tile columns
+// 0-127 and 160-287), the second (N = 64) rows [128, 160) (tile columns
+// 128-159 and 288-319).
+template <int BN>
+__device__ __forceinline__ int chunk_col(int c)
+{
+    if constexpr (BN != 320)
+        return c * kStoreCols;
+    else
+        return c < 4 ? c * 32 : (c < 8 ? 160 + (c - 4) * 32 : (c == 8 ? 128 : 288));
+}
 
 // tcgen05 shared-memory descriptor of a K-major operand tile written by TMA
 // with 128B swizzle: rows of 128 bytes (64 elements), 8-row swizzle atoms of
@@ -615,18 +638,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K-slice exchange: each slice sends the other the 32-column chunks it owns,
     // one [128 rows][32 fp32] block per chunk, into the other's idle A ring
     // Ownership of a tile's 32-column chunks by the two K slices of a cluster:
-    // with four or more chunks, pairs of adjacent chunks alternate between the
-    // slices (so each warp stores its own pair with one paired store), else
-    // single chunks do.  The chunks a CTA does not own go to consecutive slots
-    // of its staging block.  With an odd number of chunks (BN = 224) the two
-    // slices own different numbers of them.
+    // pairs of adjacent chunks alternate between the slices (so each warp
+    // stores its own pair with one paired store) up to the last multiple of
+    // four chunks, single chunks after that.  The chunks a CTA does not own go
+    // to consecutive slots of its staging block.  With an odd number of chunks
+    // (BN = 224) the two slices own different numbers of them.
     constexpr int kTileChunks = BN / kStoreCols;
-    constexpr bool kPairOwn = kTileChunks >= 4;
+    constexpr int kPairedChunks = kTileChunks - kTileChunks % 4;  // chunks owned in pairs
     constexpr int kXchgSlots = (kTileChunks + 1) / 2;
     constexpr uint32_t kXchgSlotBytes = uint32_t(kRowsPerCta) * kStoreCols * 4;
     constexpr uint32_t kXchgBytes = uint32_t(kXchgSlots) * kXchgSlotBytes;
-    auto chunk_owner = [](int c) { return kPairOwn ? ((c >> 1) & 1) : (c & 1); };
-    auto chunk_slot = [](int c) { return kPairOwn ? ((c >> 2) * 2 + (c & 1)) : (c >> 1); };
+    auto chunk_owner = [](int c) { return c < kPairedChunks ? ((c >> 1) & 1) : (c & 1); };
+    // index of c among the chunks of its owner: two per group of four in the
+    // paired region, then every other chunk
+    auto chunk_slot = [](int c) {
+        return c < kPairedChunks ? ((c >> 2) * 2 + (c & 1)) : (kPairedChunks / 2 + ((c - kPairedChunks) >> 1));
+    };
     auto owned_chunks = [&](int j) {  // chunks slice j owns
         int n = 0;
         for (int c = 0; c < kTileChunks; ++c)
@@ -882,6 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && prank == 0) {
             ptx::grid_dependency_wait();
             const uint32_t idesc = p.idesc;
+            const uint32_t idesc2 = p.idesc2;  // second MMA of a 320-column unit
             const uint64_t a_desc0 = make_sdesc_sw128(sA);
             const uint64_t b_desc0 = make_sdesc_sw128(sB);
             int stage = 0;
@@ -892,8 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
             while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusMmaTimeout)) {
-                const int buf = t & 1;
-                const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
+                const int buf = Cfg::kAccBufs == 2 ? (t & 1) : 0;
+                const uint32_t acc_phase = uint32_t(Cfg::kAccBufs == 2 ? (t >> 1) : t) & 1u;
                 ++t;
                 if (!wait_phase(bar_acc_empty + 8 * buf, acc_phase ^ 1u, p, abort_flag,
                                 kStatusMmaTimeout))
@@ -914,6 +942,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // advance 16 elements = 32 bytes along K inside the swizzle atom
                         ptx::mma_f16<CG>(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc,
                                          (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        if constexpr (Cfg::kMmaN2 > 0)
+                            ptx::mma_f16<CG>(d_tmem + uint32_t(Cfg::kMmaN1),
+                                             ad + uint64_t(kk * 2),
+                                             bd + uint64_t(((Cfg::kMmaN1 / 2) * 128) >> 4) + uint64_t(kk * 2),
+                                             idesc2, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
                     // the stage is free once every pair sharing it has read it (with
                     // A multicast both pairs of the cluster, else this pair)
@@ -961,8 +994,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusEpilogueTimeout)) {
             if (t > 0 && warp == 2 && lane == 0)
                 trace_unit(p, t - 1, 3);  // previous unit's epilogue finished
-            const int buf = t & 1;
-            const uint32_t acc_phase = uint32_t(t >> 1) & 1u;
+            const int buf = Cfg::kAccBufs == 2 ? (t & 1) : 0;
+            const uint32_t acc_phase = uint32_t(Cfg::kAccBufs == 2 ? (t >> 1) : t) & 1u;
             ++t;
             // the warp leaves together: a lane that timed out just as the phase
             // completed must not strand the others in the aligned TMEM loads
@@ -1066,9 +1099,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++c;
                         continue;
                     }
-                    const int col = n_col + c * kStoreCols;
+                    const int col = n_col + chunk_col<BN>(c);
                     uint32_t r[32];
-                    if (c + 1 < c_end && chunk_owner(c + 1) == j && pair_ok<TR>(p, col, m_row)) {
+                    if (c + 1 < c_end && chunk_owner(c + 1) == j && chunk_col<BN>(c + 1) == chunk_col<BN>(c) + 32 &&
+                        pair_ok<TR>(p, col, m_row)) {
                         pair_begin(sq, lane);
                         sum_chunk(c, r);
                         pair_stage<TR>(r, p, sq, 0, lane);
@@ -1096,9 +1130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // store, two chunks per store where they pair up
 #pragma unroll 1
                 for (int c = c_begin; c < c_end;) {
-                    const int col = n_col + c * kStoreCols;
+                    const int col = n_col + chunk_col<BN>(c);
                     uint32_t r[32];
-                    if (c + 1 < c_end && pair_ok<TR>(p, col, m_row)) {
+                    if (c + 1 < c_end && chunk_col<BN>(c + 1) == chunk_col<BN>(c) + 32 && pair_ok<TR>(p, col, m_row)) {
                         pair_begin(sq, lane);
                         ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * kStoreCols), r);
                         ptx::tmem_ld_wait();
@@ -1224,7 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             r[4 * v + 2] = __float_as_uint(acc[v].z);
                             r[4 * v + 3] = __float_as_uint(acc[v].w);
                         }
-                        store_box<TR>(r, p, &tmap_c, sq, lane, n_col + c * kStoreCols, m_row);
+                        store_box<TR>(r, p, &tmap_c, sq, lane, n_col + chunk_col<BN>(c), m_row);
                     }
                 }
                 // second arrival: the slice that completes 2S has seen every other
@@ -1331,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + sp[v].z);
                         r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + sp[v].w);
                     }
-                    store_box<TR>(r, p, &tmap_c, sq, lane, n_col + c * kStoreCols, m_row);
+                    store_box<TR>(r, p, &tmap_c, sq, lane, n_col + chunk_col<BN>(c), m_row);
                 }
                 __syncwarp();
                 if (lane == 0)

@@ -59,7 +59,8 @@ struct GemmParams {
     int32_t raster_group;   // m-blocks per raster group (>= 1)
     int64_t sk_iters;       // sk_tiles * num_k_blocks
     int32_t dtype;          // 0 = bf16, 1 = fp16 (inputs and output)
-    uint32_t idesc;         // tcgen05 instruction descriptor
+    uint32_t idesc;         // tcgen05 instruction descriptor (MMA N = min(BN, 256))
+    uint32_t idesc2;        // second MMA of a 320-column unit (N = 64), else 0
     uint64_t timeout_ns;    // bound on every device-side wait
     uint32_t* status;       // device status word
     float* partials;        // fp32 partial tiles of split-K slices / stream-K pieces

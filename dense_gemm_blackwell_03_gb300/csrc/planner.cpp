@@ -59,7 +59,8 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     int bn;
     if (opts.tile_n == 0)
         bn = swap ? (Nk <= 64 ? 64 : 128) : (Nk <= 128 ? 128 : 256);
-    else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 224 || opts.tile_n == 256)
+    else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 224 || opts.tile_n == 256 ||
+             opts.tile_n == 320)
         bn = opts.tile_n;
     else
         return BWGEMM_ERR_INVALID_ARG;
@@ -94,17 +95,17 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         return BWGEMM_ERR_INVALID_ARG;
     const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
 
-    // Tile width of the pair form: 224 instead of 256 columns when the
-    // problem fits one wave either way and 224-wide tiles occupy clearly more
-    // of the workers.  N = 8192 makes 32 tiles of 256 (x 2 K slices, or x 2
-    // row blocks: 64 of 76 pairs) but 37 of 224 (74 of 76); a memory-bound
-    // decode shape then streams its weights through 148 SMs instead of 128.
+    // Tile width of the pair form: 224 or 320 instead of 256 columns when
+    // the problem then fits one wave clearly better.  N = 8192 makes 32 tiles
+    // of 256 (x 2 K slices, or x 2 row blocks: 64 of 76 pairs) but 37 of 224
+    // (74 of 76); N = 10240 makes 40 tiles of 256 (too many for two slices
+    // each: left to stream-K) but 32 of 320, whose two slices fill 64 pairs.
     // (The occupancy follows the one-wave split rule of the schedule below.)
     if (opts.tile_n == 0 && cg == 2 && !swap && mc == 1 && bn == 256 && opts.split_k == 0 && !clc &&
         opts.schedule != BWGEMM_SCHEDULE_STREAM_K) {
-        // tiles, K slices per tile (one-wave rule of the schedule below) and
-        // the share of the workers busy; 0 slices when the launch would take
-        // more than one wave or be left to stream-K
+        // tiles, K slices per tile and the share of the workers busy in a
+        // one-wave launch of whole tiles or split-K slices; 0 slices when the
+        // launch would take more than one wave or be left to stream-K
         struct Wave {
             int64_t tiles, slices;
             double occupancy;
@@ -129,10 +130,15 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         auto clustered = [&](const Wave& w) {
             return opts.cluster_split != 1 && w.slices == 2 && w.tiles <= max_quads;
         };
-        const Wave w256 = one_wave(256), w224 = one_wave(224);
-        if (w256.occupancy > 0.0 && w224.occupancy > w256.occupancy + 0.05 &&
-            !(clustered(w256) && !clustered(w224)))
-            bn = 224;
+        const Wave w256 = one_wave(256);
+        Wave best = w256;
+        for (int b : {224, 320}) {
+            const Wave w = one_wave(b);
+            if (w.occupancy > best.occupancy + 0.05 && !(clustered(w256) && !clustered(w))) {
+                best = w;
+                bn = b;
+            }
+        }
     }
     const int idx = find_variant(cg, bn, swap, mc);
     if (idx < 0)
@@ -319,7 +325,8 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
     p.sk_iters = sel.sk_iters;
     p.raster_group = sel.cfg.raster_group;
     p.dtype = int32_t(dtype);
-    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn);
+    p.idesc = make_idesc(int(dtype), kRowsPerCta * v.cg, std::min(v.bn, 256));
+    p.idesc2 = v.bn > 256 ? make_idesc(int(dtype), kRowsPerCta * v.cg, v.bn - 256) : 0u;
     p.stall_kblock = -1;
     p.split_scatter = sel.cfg.split_scatter;
     p.prefetch = sel.cfg.prefetch_kblocks;

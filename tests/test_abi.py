@@ -151,8 +151,12 @@ def test_select_decode_shapes():
         c = cfg(256, N, K, sms=152, pairs=76, quads=38, swap_ab=1)
         assert c["tile_n"] == 224 and c["num_tiles"] == 37 and c["cluster_split"] == 1
         assert c["grid"] == 148
-    # fused QKV: 40 tiles, 2 slices would not fit one wave -> stream-K over all pairs
-    c = cfg(256, 10240, 8192, sms=152, pairs=76, swap_ab=1)
+    # fused QKV: 40 tiles of 256 -- 2 slices would not fit one wave (stream-K);
+    # 32 tiles of 320 (two MMAs per K step) x 2 slices in 32 clusters of four
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1)
+    assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
+    assert c["cluster_split"] == 1 and c["grid"] == 128 and c["stages"] == 5
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
     # MLP up: 112 tiles = 1.47 waves -> stream-K
     c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1)
@@ -162,17 +166,21 @@ def test_select_decode_shapes():
     c = cfg(512, 8192, 5376, sms=152, pairs=76)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 148
     assert c["tile_n"] == 224 and c["num_tiles"] == 74
-    # the 224-wide rule stays out of multi-wave, stream-K, forced and 1-SM cases
+    # the width rule stays out of multi-wave, stream-K, forced and 1-SM cases
     assert cfg(4096, 4096, 4096, sms=152, pairs=76)["tile_n"] == 256
-    assert cfg(256, 10240, 8192, sms=152, pairs=76)["tile_n"] == 256
+    assert cfg(256, 28672, 8192, sms=152, pairs=76)["tile_n"] == 256
+    assert cfg(256, 10240, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_STREAM_K)["tile_n"] == 256
     assert cfg(256, 8192, 8192, sms=152, pairs=76, split_k=2)["tile_n"] == 256
     assert cfg(256, 8192, 8192, sms=152, pairs=76, multicast=2)["tile_n"] == 256
     assert cfg(128, 8192, 8192, sms=152, pairs=76)["tile_n"] == 256
-    # explicit 224 exists only in the pair form with the operands in order
-    assert cfg(1000, 2000, 512, tile_n=224, variant=2)["tile_n"] == 224
-    for bad in (dict(variant=1), dict(swap_ab=2), dict(multicast=2)):
-        with pytest.raises(binding.BwgemmError):
-            cfg(1000, 2000, 512, tile_n=224, **bad)
+    # explicit 224 and 320 exist only in the pair form with the operands in order
+    for tn in (224, 320):
+        assert cfg(1000, 2000, 512, tile_n=tn, variant=2)["tile_n"] == tn
+        for bad in (dict(variant=1), dict(swap_ab=2), dict(multicast=2)):
+            with pytest.raises(binding.BwgemmError):
+                cfg(1000, 2000, 512, tile_n=tn, **bad)
+    with pytest.raises(binding.BwgemmError):
+        cfg(1000, 2000, 512, tile_n=288)
 
 
 def test_select_swapped_operands_for_small_m():
@@ -248,11 +256,14 @@ def test_select_cluster_split():
     assert c["swap_ab"] == 1 and c["cluster_split"] == 1 and c["grid"] == 64 * 2
     c = cfg(256, 8192, 8192, sms=152, pairs=76, cluster_split=1)
     assert c["cluster_split"] == 0 and c["split_scatter"] == 1 and c["workspace_bytes"] > 0
-    # 40 tiles need 40 clusters of four CTAs: more than fit at once
-    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    # 40 tiles of 256 need 40 clusters of four CTAs: more than fit at once
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, tile_n=256)
     assert c["cluster_split"] == 0
     with pytest.raises(binding.BwgemmError):
-        cfg(256, 10240, 8192, sms=152, pairs=76, cluster_split=2)
+        cfg(256, 10240, 8192, sms=152, pairs=76, cluster_split=2, tile_n=256)
+    # 32 tiles of 320 fit
+    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    assert c["tile_n"] == 320 and c["cluster_split"] == 1
     with pytest.raises(binding.BwgemmError):
         cfg(256, 8192, 8192, cluster_split=3)
 

@@ -88,7 +88,7 @@ def test_strided_operands_and_output(plan):
     assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
 
 
-@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 224), (2, 256)])
+@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 224), (2, 256), (2, 320)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_every_variant(variant, tile_n, dtype):
     A = make_matrix(520, 640, "normal", dtype, seed=800, device="cuda")
@@ -281,19 +281,35 @@ def test_tune_rejects_bad_arguments():
     dict(schedule=binding.SCHEDULE_STREAM_K, max_ctas=24),
     dict(schedule=binding.SCHEDULE_CLC),
 ])
-def test_tile224_exact(M, N, K, opts):
-    # 7 store chunks of 32 columns per tile (an odd count: the two K slices of
-    # a cluster own 4 and 3 of them), the second accumulator at TMEM column
-    # 256, ragged M, N and K; integer inputs, run twice
+@pytest.mark.parametrize("tile_n", [224, 320])
+def test_wide_tiles_exact(M, N, K, opts, tile_n):
+    # 224: 7 store chunks of 32 columns per tile (an odd count: the two K
+    # slices of a cluster own 4 and 3 of them), the second accumulator at TMEM
+    # column 256.  320: two MMAs per K step (N = 256 and N = 64) into one
+    # accumulator, its chunks mapped back to the tile's columns.  Ragged M, N
+    # and K; integer inputs, run twice
     A = make_matrix(M, K, "int2", seed=3700 + M, device="cuda")
     B = make_matrix(N, K, "int2", seed=3710 + N, device="cuda")
-    with binding.Plan(0, variant=2, tile_n=224, swap_ab=1, **opts) as p:
+    with binding.Plan(0, variant=2, tile_n=tile_n, swap_ab=1, **opts) as p:
         for _ in range(2):
             run_full(p, A, B, "bf16", exact=True)
         c = p.last_config()
-        assert c["tile_n"] == 224 and c["variant"] == 2
+        assert c["tile_n"] == tile_n and c["variant"] == 2
         if opts.get("cluster_split") == 2:
             assert c["cluster_split"] == 1
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tile320_auto_qkv_family(dtype):
+    # the planner's choice for one row block over N = 10240 (32 tiles of 320,
+    # two K slices each in one cluster) on N(0,1) activations and N(0, 0.02^2)
+    # weights
+    A = make_matrix(256, 1024, "normal", dtype, seed=3730, device="cuda")
+    B = make_matrix(10240, 1024, "weight", dtype, seed=3731, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, dtype)
+        c = p.last_config()
+        assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])

@@ -50,11 +50,12 @@ namespace bwgemm {
 template <int CG, int BN, int STAGES>
 struct KernelConfig {
     static_assert(CG == 1 || CG == 2, "CTA group is 1 or 2");
-    static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || (CG == 2 && BN == 320)),
-                  "BN in [64, 256] (multiple of 32), or 320 for the CTA pair");
+    static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || (CG == 2 && BN <= 384)),
+                  "BN in [64, 256] (multiple of 32), or up to 384 for the CTA pair");
     // columns of the first and second MMA of a K step: one MMA up to 256
-    // columns; a 320-column unit issues N = 256 and N = 64 into one 320-column
-    // accumulator, the second reading the last 32 B rows of each CTA's stage
+    // columns; a wider pair unit (320, 384) issues N = 256 and N = BN - 256
+    // into one accumulator, the second reading B rows [128, BN / 2) of each
+    // CTA's stage
     static constexpr int kMmaN1 = BN <= 256 ? BN : 256;
     static constexpr int kMmaN2 = BN - kMmaN1;
     static constexpr int kTileM = CG * kRowsPerCta;             // rows per work unit
@@ -93,17 +94,22 @@ struct KernelConfig {
 
 // Column of the tile (relative to its first column) that accumulator chunk c
 // (32 columns) holds.  Up to 256 columns the accumulator is the tile.  In a
-// 320-column unit each CTA of the pair stages B rows [0, 160) of its half;
-// the first MMA (N = 256) reads rows [0, 128) of both halves (tile columns
-// 0-127 and 160-287), the second (N = 64) rows [128, 160) (tile columns
-// 128-159 and 288-319).
+// wider pair unit each CTA stages B rows [0, H) of its half, H = BN / 2: the
+// first MMA (N = 256) reads rows [0, 128) of both halves (tile columns 0-127
+// and H..H+127), the second (N = BN - 256) rows [128, H) (tile columns
+// 128..H-1 and H+128..BN-1).  For 320: chunks 0-3, 4-7, 8, 9 hold columns
+// 0, 160, 128, 288 onwards.
 template <int BN>
 __device__ __forceinline__ int chunk_col(int c)
 {
-    if constexpr (BN != 320)
+    if constexpr (BN <= 256) {
         return c * kStoreCols;
-    else
-        return c < 4 ? c * 32 : (c < 8 ? 160 + (c - 4) * 32 : (c == 8 ? 128 : 288));
+    } else {
+        constexpr int H = BN / 2;          // B rows per CTA
+        constexpr int E = (H - 128) / 32;  // chunks of the second MMA per half
+        return c < 4 ? c * 32
+                     : (c < 8 ? H + (c - 4) * 32 : (c < 8 + E ? 128 + (c - 8) * 32 : H + 128 + (c - 8 - E) * 32));
+    }
 }
 
 // tcgen05 shared-memory descriptor of a K-major operand tile written by TMA

@@ -99,6 +99,7 @@ constexpr VariantFns kFns[] = {
     BWGEMM_VARIANT(2, 256, 6, false, 1, 2), BWGEMM_VARIANT(1, 64, 8, true, 1, 2),
     BWGEMM_VARIANT(2, 224, 6, false, 1, 1), BWGEMM_VARIANT(2, 224, 6, false, 1, 2),
     BWGEMM_VARIANT(2, 320, 5, false, 1, 1), BWGEMM_VARIANT(2, 320, 5, false, 1, 2),
+    BWGEMM_VARIANT(2, 384, 4, false, 1, 1),
 };
 #undef BWGEMM_VARIANT
 static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");

@@ -21,7 +21,8 @@ namespace bwgemm {
 // The BN = 224 pair variants cut N = 8192 into 37 column tiles, so that one
 // row block (x 2 K slices, or two row blocks) fills 74 of 76 CTA pairs; the
 // BN = 320 ones (two MMAs per K step, one 320-column accumulator) cut
-// N = 10240 into 32 tiles, whose 2 K slices fit 32 clusters of four.
+// N = 10240 into 32 tiles, whose 2 K slices fit 32 clusters of four; BN = 384
+// cuts N = 28672 into 75 tiles, one wave of whole tiles.
 struct Variant {
     int cg;      // 1: cta_group::1, 128-row units; 2: CTA pair, 256-row units
     int bn;      // columns of the MMA per unit (= MMA N)
@@ -37,7 +38,7 @@ constexpr Variant kVariants[] = {
     {1, 128, 6, true, 1, 1},  {1, 64, 8, true, 1, 1},   {2, 256, 6, false, 2, 1},
     {2, 128, 8, false, 2, 1}, {2, 256, 6, false, 1, 2}, {1, 64, 8, true, 1, 2},
     {2, 224, 6, false, 1, 1}, {2, 224, 6, false, 1, 2},
-    {2, 320, 5, false, 1, 1}, {2, 320, 5, false, 1, 2},
+    {2, 320, 5, false, 1, 1}, {2, 320, 5, false, 1, 2}, {2, 384, 4, false, 1, 1},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 

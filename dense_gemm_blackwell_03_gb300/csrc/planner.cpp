@@ -60,7 +60,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     if (opts.tile_n == 0)
         bn = swap ? (Nk <= 64 ? 64 : 128) : (Nk <= 128 ? 128 : 256);
     else if (opts.tile_n == 64 || opts.tile_n == 128 || opts.tile_n == 224 || opts.tile_n == 256 ||
-             opts.tile_n == 320)
+             opts.tile_n == 320 || opts.tile_n == 384)
         bn = opts.tile_n;
     else
         return BWGEMM_ERR_INVALID_ARG;
@@ -95,11 +95,12 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         return BWGEMM_ERR_INVALID_ARG;
     const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
 
-    // Tile width of the pair form: 224 or 320 instead of 256 columns when
-    // the problem then fits one wave clearly better.  N = 8192 makes 32 tiles
-    // of 256 (x 2 K slices, or x 2 row blocks: 64 of 76 pairs) but 37 of 224
-    // (74 of 76); N = 10240 makes 40 tiles of 256 (too many for two slices
-    // each: left to stream-K) but 32 of 320, whose two slices fill 64 pairs.
+    // Tile width of the pair form: 224, 320 or 384 instead of 256 columns
+    // when the problem then fits one wave clearly better.  N = 8192 makes 32
+    // tiles of 256 (x 2 K slices, or x 2 row blocks: 64 of 76 pairs) but 37
+    // of 224 (74 of 76); N = 10240 makes 40 tiles of 256 (too many for two
+    // slices each: left to stream-K) but 32 of 320, whose two slices fill 64
+    // pairs; N = 28672 makes 112 tiles of 256 (1.5 waves) but 75 of 384.
     // (The occupancy follows the one-wave split rule of the schedule below.)
     if (opts.tile_n == 0 && cg == 2 && !swap && mc == 1 && bn == 256 && opts.split_k == 0 && !clc &&
         opts.schedule != BWGEMM_SCHEDULE_STREAM_K) {
@@ -127,14 +128,17 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         // clusters of four CTAs; trading that exchange for the one through L2
         // measured slower than the 24 SMs it gains (decode M = 256, N = 8192:
         // 36 clusters of four fit on GB300, 37 tiles of 224 do not).
-        auto clustered = [&](const Wave& w) {
-            return opts.cluster_split != 1 && w.slices == 2 && w.tiles <= max_quads;
+        // So a narrower or wider tile is taken only as whole tiles, or with
+        // its two slices in clusters (where that width has a clustered form).
+        auto clustered = [&](const Wave& w, int b) {
+            return opts.cluster_split != 1 && w.slices == 2 && w.tiles <= max_quads &&
+                   find_variant(2, b, false, 1, 2) >= 0;
         };
         const Wave w256 = one_wave(256);
         Wave best = w256;
-        for (int b : {224, 320}) {
+        for (int b : {224, 320, 384}) {
             const Wave w = one_wave(b);
-            if (w.occupancy > best.occupancy + 0.05 && !(clustered(w256) && !clustered(w))) {
+            if (w.occupancy > best.occupancy + 0.05 && (w.slices < 2 || clustered(w, b))) {
                 best = w;
                 bn = b;
             }

@@ -78,10 +78,10 @@ typedef enum {
  * defaults with bwgemm_default_options(). */
 typedef struct {
     int32_t variant;          /* bwgemm_variant_t                                       */
-    int32_t tile_n;           /* 0 = auto, 64, 128, 224, 256 or 320: columns per work
-                                 unit (224 and 320: CTA-pair form, operands not
-                                 swapped, no multicast; 320 issues two MMAs, N = 256
-                                 and N = 64, into one accumulator)                      */
+    int32_t tile_n;           /* 0 = auto, 64, 128, 224, 256, 320 or 384: columns per
+                                 work unit (224, 320, 384: CTA-pair form, operands not
+                                 swapped, no multicast; 320 and 384 issue two MMAs,
+                                 N = 256 and N = tile_n - 256, into one accumulator)    */
     int32_t split_k;          /* 0 = auto, 1 = off, s >= 2: s K-slices per tile         */
     int32_t raster_group;     /* 0 = auto; m-blocks walked before stepping along N      */
     int32_t max_ctas;         /* 0 = fill the GPU; else cap on the persistent grid      */

@@ -158,9 +158,16 @@ def test_select_decode_shapes():
     assert c["cluster_split"] == 1 and c["grid"] == 128 and c["stages"] == 5
     c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
-    # MLP up: 112 tiles = 1.47 waves -> stream-K
+    # MLP up: 112 tiles of 256 = 1.47 waves (stream-K); 75 tiles of 384 (two
+    # MMAs per K step) = one wave of whole tiles
     c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1)
+    assert c["tile_n"] == 384 and c["num_tiles"] == 75 and c["split_k"] == 1
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["grid"] == 150 and c["stages"] == 4
+    c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["dp_tiles"] == 0
+    # a wider tile whose split would reduce through L2 is not taken: 32 tiles
+    # of 384 x 2 slices (no clustered form of 384) -> 256 and stream-K
+    assert cfg(256, 12288, 8192, sms=152, pairs=76, quads=36)["tile_n"] == 256
     # Gemma-like 512 x 8192 x 5376: 2 x 37 tiles of 224 fill 74 of 76 pairs
     # (2 x 32 of 256 would fill 64) -> whole tiles of 224
     c = cfg(512, 8192, 5376, sms=152, pairs=76)
@@ -168,13 +175,13 @@ def test_select_decode_shapes():
     assert c["tile_n"] == 224 and c["num_tiles"] == 74
     # the width rule stays out of multi-wave, stream-K, forced and 1-SM cases
     assert cfg(4096, 4096, 4096, sms=152, pairs=76)["tile_n"] == 256
-    assert cfg(256, 28672, 8192, sms=152, pairs=76)["tile_n"] == 256
+    assert cfg(8192, 28672, 8192, sms=152, pairs=76)["tile_n"] == 256
     assert cfg(256, 10240, 8192, sms=152, pairs=76, schedule=binding.SCHEDULE_STREAM_K)["tile_n"] == 256
     assert cfg(256, 8192, 8192, sms=152, pairs=76, split_k=2)["tile_n"] == 256
     assert cfg(256, 8192, 8192, sms=152, pairs=76, multicast=2)["tile_n"] == 256
     assert cfg(128, 8192, 8192, sms=152, pairs=76)["tile_n"] == 256
     # explicit 224 and 320 exist only in the pair form with the operands in order
-    for tn in (224, 320):
+    for tn in (224, 320, 384):
         assert cfg(1000, 2000, 512, tile_n=tn, variant=2)["tile_n"] == tn
         for bad in (dict(variant=1), dict(swap_ab=2), dict(multicast=2)):
             with pytest.raises(binding.BwgemmError):

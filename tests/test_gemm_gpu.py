@@ -88,7 +88,8 @@ def test_strided_operands_and_output(plan):
     assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
 
 
-@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 224), (2, 256), (2, 320)])
+@pytest.mark.parametrize("variant,tile_n", [(1, 128), (1, 256), (2, 128), (2, 224), (2, 256), (2, 320),
+                                            (2, 384)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_every_variant(variant, tile_n, dtype):
     A = make_matrix(520, 640, "normal", dtype, seed=800, device="cuda")
@@ -281,13 +282,16 @@ def test_tune_rejects_bad_arguments():
     dict(schedule=binding.SCHEDULE_STREAM_K, max_ctas=24),
     dict(schedule=binding.SCHEDULE_CLC),
 ])
-@pytest.mark.parametrize("tile_n", [224, 320])
+@pytest.mark.parametrize("tile_n", [224, 320, 384])
 def test_wide_tiles_exact(M, N, K, opts, tile_n):
     # 224: 7 store chunks of 32 columns per tile (an odd count: the two K
     # slices of a cluster own 4 and 3 of them), the second accumulator at TMEM
     # column 256.  320: two MMAs per K step (N = 256 and N = 64) into one
     # accumulator, its chunks mapped back to the tile's columns.  Ragged M, N
-    # and K; integer inputs, run twice
+    # and K; integer inputs, run twice.  384: N = 256 and N = 128, no
+    # clustered split form.
+    if tile_n == 384 and opts.get("cluster_split") == 2:
+        pytest.skip("no clustered split-K form of 384-column units")
     A = make_matrix(M, K, "int2", seed=3700 + M, device="cuda")
     B = make_matrix(N, K, "int2", seed=3710 + N, device="cuda")
     with binding.Plan(0, variant=2, tile_n=tile_n, swap_ab=1, **opts) as p:
@@ -310,6 +314,18 @@ def test_tile320_auto_qkv_family(dtype):
         run_full(p, A, B, dtype)
         c = p.last_config()
         assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tile384_auto_mlp_up_family(dtype):
+    # the planner's choice for one row block over N = 28672 (75 whole tiles
+    # of 384, one wave) on N(0,1) activations and N(0, 0.02^2) weights
+    A = make_matrix(256, 512, "normal", dtype, seed=3740, device="cuda")
+    B = make_matrix(28672, 512, "weight", dtype, seed=3741, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, dtype)
+        c = p.last_config()
+        assert c["tile_n"] == 384 and c["num_tiles"] == 75 and c["split_k"] == 1
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])

@@ -6,8 +6,9 @@
 // Structure (one CTA per SM, or one CTA pair per two SMs when CG == 2):
 //   warp 0      TMA producer: fills a STAGES-deep ring of 64-wide K blocks of A
 //               and B (128B-swizzled), guarded by full/empty mbarrier pairs.
-//   warp 1      TMEM allocator; lane 0 (of the leader CTA) issues every
-//               tcgen05.mma and commits stage release / accumulator-ready.
+//   warp 1      TMEM allocator; in the leader CTA the whole warp walks the
+//               K blocks and one elected lane issues every tcgen05.mma and
+//               commits stage release / accumulator-ready.
 //   warps 2..9  epilogue (two per TMEM lane quarter, half the columns each):
 //               tcgen05.ld -> fp32 -> bf16/fp16 -> swizzled smem -> TMA store,
 //               double-buffered per warp.  A unit that covers only part of a
@@ -848,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rel = kb - w.kb0;
                 const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 && first_unit &&
                                    p.stall_kblock >= rel && p.stall_kblock < rel + nkb;
-                if (!stall && lane == 0) {
+                if (!stall && ptx::elect_one()) {
                     if (first_unit && kb == w.kb0)
                         trace_mark(p, kTraceFirstLoad);
                     const uint32_t fb = bar_full + 8 * stage;
@@ -912,12 +913,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             trace_mark(p, kTraceLastLoad);
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        if (lane == 0 && prank == 0) {
+        // The whole warp of the pair leader walks the unit and K-block
+        // sequence (warp-uniform state) and one elected lane issues the MMAs
+        // and commits.  Issued by `lane == 0` inside a one-thread branch, each
+        // tcgen05.mma cost ~40 ns of issue (160-190 ns per K block of four),
+        // which paced the tensor pipe below its rate; elected, ~15 ns.
+        if (prank == 0) {
             ptx::grid_dependency_wait();
             const uint32_t idesc = p.idesc;
-            const uint32_t idesc2 = p.idesc2;  // second MMA of a 320-column unit
+            const uint32_t idesc2 = p.idesc2;  // second MMA of a 320/384-column unit
             const uint64_t a_desc0 = make_sdesc_sw128(sA);
             const uint64_t b_desc0 = make_sdesc_sw128(sB);
+            const uint32_t tmem0 = __shfl_sync(0xffffffffu, tmem_base, 0);
             int stage = 0;
             uint32_t phase = 0;
             int t = 0;
@@ -925,43 +932,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             Sched iter;
             iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
-            while (ok && iter.next<CG>(p, w, true, abort_flag, kStatusMmaTimeout)) {
+            while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusMmaTimeout)) {
                 const int buf = Cfg::kAccBufs == 2 ? (t & 1) : 0;
                 const uint32_t acc_phase = uint32_t(Cfg::kAccBufs == 2 ? (t >> 1) : t) & 1u;
                 ++t;
-                if (!wait_phase(bar_acc_empty + 8 * buf, acc_phase ^ 1u, p, abort_flag,
-                                kStatusMmaTimeout))
+                ok = __all_sync(0xffffffffu, wait_phase(bar_acc_empty + 8 * buf, acc_phase ^ 1u, p, abort_flag,
+                                                        kStatusMmaTimeout));
+                if (!ok)
                     break;
                 ptx::tc_fence_after_sync();
-                trace_unit(p, t - 1, 0);
-                const uint32_t d_tmem = tmem_base + uint32_t(buf * Cfg::kAccStride);
+                if (lane == 0)
+                    trace_unit(p, t - 1, 0);
+                const uint32_t d_tmem = tmem0 + uint32_t(buf * Cfg::kAccStride);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_phase(bar_full + 8 * stage, phase, p, abort_flag, kStatusMmaTimeout)) {
-                        ok = false;
+                    ok = __all_sync(0xffffffffu, wait_phase(bar_full + 8 * stage, phase, p, abort_flag,
+                                                            kStatusMmaTimeout));
+                    if (!ok)
                         break;
-                    }
                     ptx::tc_fence_after_sync();
                     const uint64_t ad = a_desc0 + uint64_t((stage * Cfg::kABytes) >> 4);
                     const uint64_t bd = b_desc0 + uint64_t((stage * Cfg::kBBytes) >> 4);
+                    if (ptx::elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
-                        // advance 16 elements = 32 bytes along K inside the swizzle atom
-                        ptx::mma_f16<CG>(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc,
-                                         (kb > w.kb0 || kk > 0) ? 1u : 0u);
-                        if constexpr (Cfg::kMmaN2 > 0)
-                            ptx::mma_f16<CG>(d_tmem + uint32_t(Cfg::kMmaN1),
-                                             ad + uint64_t(kk * 2),
-                                             bd + uint64_t(((Cfg::kMmaN1 / 2) * 128) >> 4) + uint64_t(kk * 2),
-                                             idesc2, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
+                            // advance 16 elements = 32 bytes along K inside the swizzle atom
+                            ptx::mma_f16<CG>(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc,
+                                             (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                            if constexpr (Cfg::kMmaN2 > 0)
+                                ptx::mma_f16<CG>(d_tmem + uint32_t(Cfg::kMmaN1), ad + uint64_t(kk * 2),
+                                                 bd + uint64_t(((Cfg::kMmaN1 / 2) * 128) >> 4) +
+                                                     uint64_t(kk * 2),
+                                                 idesc2, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        }
+                        // the stage is free once every pair sharing it has read it (with
+                        // A multicast both pairs of the cluster, else this pair)
+                        if constexpr (CG == 1)
+                            ptx::mma_commit(bar_empty + 8 * stage);
+                        else if constexpr (MC > 1)
+                            ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t((1u << CS) - 1u));
+                        else
+                            ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t(0x3u << (CG * pair)));
                     }
-                    // the stage is free once every pair sharing it has read it (with
-                    // A multicast both pairs of the cluster, else this pair)
-                    if constexpr (CG == 1)
-                        ptx::mma_commit(bar_empty + 8 * stage);
-                    else if constexpr (MC > 1)
-                        ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t((1u << CS) - 1u));
-                    else
-                        ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t(0x3u << (CG * pair)));
+                    __syncwarp();
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -969,11 +981,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
-                if constexpr (CG == 1)
-                    ptx::mma_commit(bar_acc_full + 8 * buf);
-                else
-                    ptx::mma_commit_pair(bar_acc_full + 8 * buf, uint16_t(0x3u << (CG * pair)));
-                trace_unit(p, t - 1, 1);
+                // the same elected lane: a commit tracks the MMAs its own thread issued
+                if (ptx::elect_one()) {
+                    if constexpr (CG == 1)
+                        ptx::mma_commit(bar_acc_full + 8 * buf);
+                    else
+                        ptx::mma_commit_pair(bar_acc_full + 8 * buf, uint16_t(0x3u << (CG * pair)));
+                }
+                __syncwarp();
+                if (lane == 0)
+                    trace_unit(p, t - 1, 1);
             }
         }
     } else {

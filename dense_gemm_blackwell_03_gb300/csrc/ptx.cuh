@@ -90,6 +90,26 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
                  : "memory");
 }
 
+// True in exactly one lane of the (fully converged) warp, the same lane at every
+// call.  Issuing a single-thread instruction (TMA copy, tcgen05.mma / commit)
+// under this predicate instead of `lane == 0` lets the compiler treat the
+// region as one thread, so operands already held warp-uniformly are not
+// re-checked lane by lane before each issue.  Per-thread state (the MMAs a
+// tcgen05.commit tracks) stays with that one lane because the choice is fixed
+// for a given member mask.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t"
+        ".reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t"
+        "}"
+        : "+r"(pred));
+    return pred != 0;
+}
+
 // One probe of the phase with the given parity; true once that phase completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {

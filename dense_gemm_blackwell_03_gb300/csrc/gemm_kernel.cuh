@@ -78,8 +78,8 @@ struct KernelConfig {
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
     // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4],
-    // exchange_ready, exchange_full, exchange_staged
-    static constexpr int kNumBars = 2 * STAGES + 7 + 2 * kClcSlots;
+    // exchange_ready, exchange_full[2], exchange_staged[2]
+    static constexpr int kNumBars = 2 * STAGES + 9 + 2 * kClcSlots;
     // 16-byte responses on 16-byte boundaries (the barrier count may be odd)
     static constexpr int kOffClcResp = (kOffBar + kNumBars * 8 + 15) & ~15;
     static constexpr int kOffTmemSlot = kOffClcResp + 16 * kClcSlots;
@@ -661,12 +661,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto chunk_slot = [](int c) {
         return c < kPairedChunks ? ((c >> 2) * 2 + (c & 1)) : (kPairedChunks / 2 + ((c - kPairedChunks) >> 1));
     };
-    auto owned_chunks = [&](int j) {  // chunks slice j owns
-        int n = 0;
-        for (int c = 0; c < kTileChunks; ++c)
-            n += (chunk_owner(c) == j) ? 1 : 0;
-        return n;
-    };
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kABytes, "exchange fits the A ring");
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kBBytes, "staging fits the B ring");
     extern __shared__ uint8_t smem_raw[];
@@ -693,8 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_clc_full = bar_acc_empty + 16;      // + 8 * slot
     const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots;  // + 8 * slot (leader's counts)
     const uint32_t bar_xready = bar_clc_empty + 8 * kClcSlots;    // the other slice's ring is free
-    const uint32_t bar_xfull = bar_xready + 8;                    // the other slice's chunks landed
-    const uint32_t bar_xstaged = bar_xfull + 8;                   // every epilogue warp staged its rows
+    const uint32_t bar_xfull = bar_xready + 8;      // + 8 * half: the other slice's chunks landed
+    const uint32_t bar_xstaged = bar_xfull + 16;    // + 8 * half: the half's four warps staged their rows
     const uint32_t clc_resp = base + Cfg::kOffClcResp;     // + 16 * slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
@@ -715,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_clc_empty + 8 * s, CS * (1 + kEpiWarps) + CS / CG);
         }
         ptx::mbar_init(bar_xready, 1);  // the partner's arrival
-        ptx::mbar_init(bar_xfull, 1);   // own arrive.expect_tx; the partner's bulk-copy bytes
-        ptx::mbar_init(bar_xstaged, kEpiWarps);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(bar_xfull + 8 * h, 1);  // own arrive.expect_tx; the partner's bulk-copy bytes
+            ptx::mbar_init(bar_xstaged + 8 * h, kEpiWarps / 2);
+        }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -754,7 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         // The whole warp walks the unit and K-block sequence, so the loop state
-        // is warp-uniform, and lane 0 issues the copies and barrier updates.
+        // is warp-uniform, and one elected lane issues the copies and barrier
+        // updates.
         // (Run by lane 0 alone, every TMA instruction first moved its
         // per-thread operands into uniform registers; that bookkeeping cost
         // more than a K block's MMAs and left the tensor pipe waiting.)
@@ -1036,14 +1033,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- split-K inside the cluster: the two K slices of this tile
                 // run on the two pairs (or CTAs) of the cluster.  Chunk c belongs
                 // to slice chunk_owner(c).  Each CTA stages the chunks its partner (same
-                // rank in the other slice) owns in its own idle B ring (one
-                // contiguous block); once every epilogue warp has staged its rows,
-                // one thread tells the partner that this CTA's A ring is free and,
-                // once the partner's is free, copies the whole block into it with
-                // one bulk copy (counted on the partner's exchange barrier); then
-                // every warp waits for its own chunks and stores own + partner's
-                // in C.  One tile per cluster (the planner's one-wave rule), so no
-                // later unit refills the ring.  Warps whose rows are all past M
+                // rank in the other slice) owns in its own idle B ring; the
+                // exchange runs in two halves, one per column half of the epilogue
+                // warps (h), whose staged chunks are contiguous in the block.  As
+                // soon as the unit's MMAs are done (the rings are idle) one thread
+                // tells the partner that this CTA's A ring may be written; once a
+                // half's four warps have staged their rows and the partner's ring is
+                // free, the half's first warp copies that half into it with one bulk
+                // copy, counted on the partner's barrier of that half.  Each warp
+                // then waits only for its half of the partner's chunks and stores
+                // own + partner's in C.  One tile per cluster (the planner's one-wave rule), so no
+                // later unit refills the rings.  Warps whose rows are all past M
                 // take part too (the byte counts cover every row); their rows are
                 // clipped.  (Per-thread st.async remote stores measured ~3 GB/s
                 // per warp; a bulk copy per warp and chunk was fast but each copy
@@ -1057,12 +1057,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return uint32_t(chunk_slot(c) * (kRowsPerCta * kStoreCols * 4) + row * (kStoreCols * 4)) +
                            ((uint32_t(v) ^ swz) << 4);
                 };
-                bool owns_any = false;
-                int last_owned = c_begin;
+                // chunks of half hh that slice jj owns, and the slot of the first one
+                auto half_owned = [&](int jj, int hh) {
+                    int n = 0;
+                    for (int c = hh * kHalfChunks; c < (hh ? kTileChunks : kHalfChunks); ++c)
+                        n += (chunk_owner(c) == jj) ? 1 : 0;
+                    return n;
+                };
+                auto half_first_slot = [&](int jj, int hh) {
+                    for (int c = hh * kHalfChunks; c < (hh ? kTileChunks : kHalfChunks); ++c)
+                        if (chunk_owner(c) == jj)
+                            return chunk_slot(c);
+                    return 0;
+                };
+                if (warp == 2 && lane == 0) {
+                    // the bytes each half receives, then: this CTA's A ring is free
+                    ptx::mbar_arrive_expect_tx(bar_xfull, uint32_t(half_owned(j, 0)) * kXchgSlotBytes);
+                    ptx::mbar_arrive_expect_tx(bar_xfull + 8, uint32_t(half_owned(j, 1)) * kXchgSlotBytes);
+                    ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
+                }
+                int first_owned = c_end, last_owned = c_begin;
 #pragma unroll 1
                 for (int c = c_begin; c < c_end; ++c) {
                     if (chunk_owner(c) == j) {
-                        owns_any = true;
+                        first_owned = min(first_owned, c);
                         last_owned = c;
                         continue;
                     }
@@ -1073,30 +1091,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int v = 0; v < 8; ++v)
                         ptx::st_shared_v4(sB + xoff(c, v), r[4 * v + 0], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
                 }
-                if (!owns_any)
-                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                 ptx::fence_proxy_async_smem();  // the staged rows, visible to the bulk copy
                 __syncwarp();
                 if (lane == 0)
-                    ptx::mbar_arrive(bar_xstaged);
-                if (warp == 2) {
-                    if (!__all_sync(0xffffffffu, wait_phase(bar_xstaged, xparity, p, abort_flag,
+                    ptx::mbar_arrive(bar_xstaged + 8 * h);
+                if (first_owned >= c_end)
+                    release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
+                if (ew == 4 * h) {
+                    // the half's first warp sends the half
+                    if (!__all_sync(0xffffffffu, wait_phase(bar_xstaged + 8 * h, xparity, p, abort_flag,
                                                             kStatusSplitTimeout)))
                         break;
-                    if (lane == 0) {
-                        // the partner sends the chunks this slice owns
-                        ptx::mbar_arrive_expect_tx(bar_xfull, uint32_t(owned_chunks(j)) * kXchgSlotBytes);
-                        ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_xready, partner));
-                    }
                     if (!__all_sync(0xffffffffu, wait_phase(bar_xready, xparity, p, abort_flag,
                                                             kStatusSplitTimeout)))
                         break;
-                    if (lane == 0)
-                        ptx::bulk_copy_to_cluster(ptx::map_to_cta(sA, partner), sB,
-                                                  uint32_t(owned_chunks(1 - j)) * kXchgSlotBytes,
-                                                  ptx::map_to_cta(bar_xfull, partner));
+                    const int n_send = half_owned(1 - j, h);
+                    if (lane == 0 && n_send > 0) {
+                        const uint32_t off = uint32_t(half_first_slot(1 - j, h)) * kXchgSlotBytes;
+                        ptx::bulk_copy_to_cluster(ptx::map_to_cta(sA + off, partner), sB + off,
+                                                  uint32_t(n_send) * kXchgSlotBytes,
+                                                  ptx::map_to_cta(bar_xfull + 8 * h, partner));
+                    }
                 }
-                if (!__all_sync(0xffffffffu, wait_phase(bar_xfull, xparity, p, abort_flag,
+                if (!__all_sync(0xffffffffu, wait_phase(bar_xfull + 8 * h, xparity, p, abort_flag,
                                                         kStatusSplitTimeout)))
                     break;
                 // own chunk c: this slice's partial from TMEM + the partner's
@@ -1117,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(x[i]));
                 };
 #pragma unroll 1
-                for (int c = c_begin; c < c_end;) {
+                for (int c = first_owned; c < c_end;) {
                     if (chunk_owner(c) != j) {
                         ++c;
                         continue;

@@ -929,7 +929,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             Sched iter;
             iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
             WorkUnit w;
-            while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusMmaTimeout)) {
+            // Without launch control the unit sequence is pure arithmetic (a few
+            // dependent integer divisions, ~0.5 us): the next unit is worked out
+            // right after the current unit's first K block is issued, while the
+            // tensor pipe is busy, instead of between units, where it left the
+            // pipe idle.  With launch control it waits for a response and stays
+            // between units.
+            const bool ahead = !p.clc;
+            bool have = iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusMmaTimeout);
+            WorkUnit w_next;
+            bool have_next = false;
+            while (ok && have) {
                 const int buf = Cfg::kAccBufs == 2 ? (t & 1) : 0;
                 const uint32_t acc_phase = uint32_t(Cfg::kAccBufs == 2 ? (t >> 1) : t) & 1u;
                 ++t;
@@ -971,6 +981,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::mma_commit_pair(bar_empty + 8 * stage, uint16_t(0x3u << (CG * pair)));
                     }
                     __syncwarp();
+                    if (ahead && kb == w.kb0)
+                        have_next = iter.next<CG, true>(p, w_next, lane == 0, abort_flag, kStatusMmaTimeout);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -988,6 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     trace_unit(p, t - 1, 1);
+                if (!ahead || w.kb0 >= w.kb1)  // (a unit without K blocks did not work it out)
+                    have_next = iter.next<CG, true>(p, w_next, lane == 0, abort_flag, kStatusMmaTimeout);
+                w = w_next;
+                have = have_next;
             }
         }
     } else {

@@ -487,6 +487,24 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, target_s=args.cpu_seconds)
 
+    # The nominal dense peak from a measured per-SM tensor rate (a tcgen05.mma
+    # probe timed in SM cycles) x SMs x the maximum SM clock; the fraction
+    # against it is printed beside the one against the measured cuBLAS peak.
+    if rank == 0 and roof["bound"] == "tensor":
+        try:
+            rate, sms = binding.probe_tensor_rate(local_rank)
+            max_mhz = clocks.get("sm_max_mhz") if isinstance(clocks, dict) else None
+            nominal = {"flop_per_clock_per_sm": round(rate, 1), "sms": sms, "sm_max_mhz": max_mhz,
+                       "source": "bwgemm_probe_tensor_rate: tcgen05.mma M=128 N=256 K=16 timed in "
+                                 "SM cycles on every SM; peak = SMs x rate x max SM clock"}
+            if max_mhz:
+                peak = sms * rate * max_mhz * 1e6 / 1e12
+                nominal["peak_tflops"] = round(peak, 1)
+                nominal["frac"] = round(value / world / peak, 4)
+        except binding.BwgemmError as e:
+            nominal = {"unavailable": str(e)}
+        roofline["nominal"] = nominal
+
     if rank == 0:
         line = {
             "metric": METRIC,

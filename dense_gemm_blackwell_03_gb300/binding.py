@@ -37,6 +37,7 @@ EXPORTED = [
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
     "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
     "bwgemm_plan_read_trace", "bwgemm_tune", "bwgemm_plan_tuned_count",
+    "bwgemm_probe_tensor_rate",
 ]
 
 # timeline slots of bwgemm_plan_read_trace
@@ -168,6 +169,9 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_status_string.restype = ctypes.c_char_p
         lib.bwgemm_version.argtypes = []
         lib.bwgemm_version.restype = i32
+        lib.bwgemm_probe_tensor_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                                 ctypes.POINTER(i32)]
+        lib.bwgemm_probe_tensor_rate.restype = st
         _lib = lib
         return lib
 
@@ -213,6 +217,18 @@ def select_config(num_sms: int, M: int, N: int, K: int, dtype: int = BF16, max_p
     if rc != 0:
         raise BwgemmError(rc, "bwgemm_select_config")
     return cfg.as_dict()
+
+
+def probe_tensor_rate(device: int = 0):
+    """(FLOP per SM clock of one SM's tensor pipe, SM count), measured on `device`
+    by bwgemm_probe_tensor_rate."""
+    lib = load_library()
+    rate = ctypes.c_double(0.0)
+    sms = ctypes.c_int32(0)
+    rc = lib.bwgemm_probe_tensor_rate(int(device), ctypes.byref(rate), ctypes.byref(sms))
+    if rc != 0:
+        raise BwgemmError(rc, "bwgemm_probe_tensor_rate")
+    return rate.value, sms.value
 
 
 def check_args(A_ptr, B_ptr, C_ptr, M, N, K, lda, ldb, ldc, dtype=BF16) -> int:

@@ -245,6 +245,21 @@ bwgemm_status_t bwgemm_plan_read_trace(bwgemm_plan_t plan, uint64_t* out, int64_
 uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);
 
 /*
+ * Dense tensor-pipe rate of one SM, measured: one CTA per SM of `device`
+ * issues 4096 tcgen05.mma (M = 128, N = 256, K = 16, bf16 in, fp32 in TMEM)
+ * on operands held in shared memory and times them in SM cycles.  Writes
+ * the median FLOP per SM clock to *flop_per_clock_per_sm and the device's
+ * SM count to *sm_count, from which a nominal dense peak is
+ * SMs x rate x clock ("Matrix Multiplication on NVIDIA's Blackwell",
+ * Kernel 2, and the CuTeDSL post's MMA step define the instruction; the
+ * pages state no per-SM rate).  Synchronises the device.  Errors:
+ * BWGEMM_ERR_INVALID_ARG (NULL output), BWGEMM_ERR_NO_DEVICE,
+ * BWGEMM_ERR_UNSUPPORTED (not sm_103), BWGEMM_ERR_CUDA, BWGEMM_ERR_TIMEOUT
+ * (the bounded wait for the MMAs ran out).
+ */
+bwgemm_status_t bwgemm_probe_tensor_rate(int device, double* flop_per_clock_per_sm, int32_t* sm_count);
+
+/*
  * Shape-keyed tuning ("Matrix Multiplication on NVIDIA's Blackwell", the
  * Gemma-shape experiment, chooses pipeline and MMA shapes per shape with an
  * autotuner).  Times a fixed list of candidate configurations -- the plan's

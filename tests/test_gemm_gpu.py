@@ -645,3 +645,27 @@ def test_cuda_graph_capture_and_replay():
             torch.cuda.synchronize()
             assert p.status() == 0
             compare(bits_of(C), oracle.gemm(bits_of(A), bits_of(B), "bf16"), "bf16", 1024, exact=True)
+
+
+def test_probe_tensor_rate():
+    """The per-SM tensor rate behind the nominal dense peak: a whole number of
+    FLOP per SM clock in a plausible range, on every SM of the device, and a
+    nominal peak at the top SM clock that is not below what cuBLAS reaches on
+    this part (the measured burst figure, where the driver recorded one)."""
+    import json
+    import os
+    import subprocess
+    rate, sms = binding.probe_tensor_rate(0)
+    assert sms == torch.cuda.get_device_properties(0).multi_processor_count
+    assert 2048.0 <= rate <= 16384.0
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    try:
+        out = subprocess.run(["nvidia-smi", "--id=0", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=30).stdout.strip()
+        max_mhz = float(out.splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        pytest.skip("nvidia-smi clocks unavailable")
+    if os.path.exists(path):
+        measured = json.load(open(path)).get("bf16_tflops")
+        if measured:
+            assert sms * rate * max_mhz * 1e6 / 1e12 >= 0.95 * float(measured)

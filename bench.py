@@ -457,8 +457,12 @@ def run_ours(args):
         xsampler.start()
         windows = {}
 
-        for name in EXTRA_SHAPES:
-            s = SHAPES[name]
+        extra = [SHAPES[n] for n in EXTRA_SHAPES]
+        if args.fp16_extra:
+            # the same shapes in fp16 (inputs rounded from the same fp32 draws)
+            extra += [SHAPES[n].with_dtype("fp16") for n in EXTRA_SHAPES if SHAPES[n].dtype != "fp16"]
+        for s in extra:
+            name = s.name
             ssets = input_sets(s, device, l2_bytes, max_sets=3)
             t, windows[name] = steady(ours, ssets)
             if plan.status(stream) != 0:
@@ -557,6 +561,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--shape", default=HEADLINE)
     ap.add_argument("--no-extra", action="store_true", help="skip the pages' other shapes")
+    ap.add_argument("--fp16-extra", action="store_true",
+                    help="also time every other shape in fp16 (adds about a minute)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -68,6 +68,11 @@ def test_version_and_status_strings(lib):
     assert lib.bwgemm_status_string(99) == b"unknown status"
 
 
+def test_probe_tensor_rate_rejects_null_outputs(lib):
+    # argument check before any device access (no GPU needed)
+    assert lib.bwgemm_probe_tensor_rate(0, None, None) == 1  # BWGEMM_ERR_INVALID_ARG
+
+
 def test_default_options(lib):
     o = PlanOptions()
     lib.bwgemm_default_options(ctypes.byref(o))

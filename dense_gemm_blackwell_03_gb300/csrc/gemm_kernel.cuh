@@ -48,7 +48,10 @@
 
 namespace bwgemm {
 
-template <int CG, int BN, int STAGES>
+// RING_STORE: the epilogue stages its output boxes in the (idle) B ring
+// instead of a region of its own -- the clustered split-K kernels, whose one
+// unit per CTA ends with idle rings; the freed region buys another stage.
+template <int CG, int BN, int STAGES, bool RING_STORE = false>
 struct KernelConfig {
     static_assert(CG == 1 || CG == 2, "CTA group is 1 or 2");
     static_assert(BN % 32 == 0 && BN >= 64 && (BN <= 256 || (CG == 2 && BN <= 384)),
@@ -76,7 +79,7 @@ struct KernelConfig {
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
-    static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
+    static constexpr int kOffBar = kOffStore + (RING_STORE ? 0 : kEpiWarps * 2 * kStoreBufBytes);
     // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4],
     // exchange_ready, exchange_full[2], exchange_staged[2]
     static constexpr int kNumBars = 2 * STAGES + 9 + 2 * kClcSlots;
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_c2,
                 const GemmParams p)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES>;
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
     static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
     static_assert(KS == 1 || (KS == 2 && MC == 1), "a cluster holds column groups or K slices");
     constexpr int CS = CG * MC * KS;  // CTAs per cluster
@@ -662,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return c < kPairedChunks ? ((c >> 2) * 2 + (c & 1)) : (kPairedChunks / 2 + ((c - kPairedChunks) >> 1));
     };
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kABytes, "exchange fits the A ring");
-    static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kBBytes, "staging fits the B ring");
+    static_assert(KS == 1 || int(kXchgBytes) + kEpiWarps * 2 * Cfg::kStoreBufBytes <= STAGES * Cfg::kBBytes,
+                  "the exchange staging and the output boxes fit the B ring");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1019,7 +1023,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c_begin = h * kHalfChunks;
         const int c_end = h ? BN / kStoreCols : kHalfChunks;
         const int row = q * 32 + lane;
-        StoreQueue sq{sStore + uint32_t(ew * 2 * Cfg::kStoreBufBytes), 0, false};
+        // the clustered split stages its output boxes in the B ring after the
+        // exchange block (its one unit ends with the rings idle)
+        const uint32_t store_base = (KS > 1) ? sB + kXchgBytes : sStore;
+        StoreQueue sq{store_base + uint32_t(ew * 2 * Cfg::kStoreBufBytes), 0, false};
         constexpr size_t kSlotF4 = size_t(Cfg::kPartialFloats) / 4;  // float4s per CTA partial
         float4* const parts = reinterpret_cast<float4*>(p.partials);
         int t = 0;
@@ -1172,6 +1179,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++c;
                     }
                 }
+                continue;
+            }
+            if constexpr (KS > 1) {
+                // a clustered split-K kernel runs split units only (its output
+                // boxes live in the B ring, which a unit without the exchange
+                // would still be loading): anything else is a planning error
+                if (lane == 0)
+                    atomicOr(p.status, kStatusBadConfig);
+                release_accumulator<CG>(bar_acc_empty + 8 * buf, lane, leader);
                 continue;
             }
 

@@ -11,7 +11,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
                        const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES>;
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
     auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -44,7 +44,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
 template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
 cudaError_t max_active_one(int* out)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES>;
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
     auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -87,7 +87,7 @@ struct VariantFns {
 
 #define BWGEMM_VARIANT(CG, BN, ST, TR, MC, KS)                                      \
     {&launch_one<CG, BN, ST, TR, MC, KS>, &max_active_one<CG, BN, ST, TR, MC, KS>, \
-     KernelConfig<CG, BN, ST>::kSmemBytes}
+     KernelConfig<CG, BN, ST, (KS > 1)>::kSmemBytes}
 
 // same order as kVariants in internal.h
 constexpr VariantFns kFns[] = {
@@ -96,9 +96,9 @@ constexpr VariantFns kFns[] = {
     BWGEMM_VARIANT(2, 128, 8, true, 1, 1),  BWGEMM_VARIANT(2, 64, 9, true, 1, 1),
     BWGEMM_VARIANT(1, 128, 6, true, 1, 1),  BWGEMM_VARIANT(1, 64, 8, true, 1, 1),
     BWGEMM_VARIANT(2, 256, 6, false, 2, 1), BWGEMM_VARIANT(2, 128, 8, false, 2, 1),
-    BWGEMM_VARIANT(2, 256, 6, false, 1, 2), BWGEMM_VARIANT(1, 64, 8, true, 1, 2),
-    BWGEMM_VARIANT(2, 224, 6, false, 1, 1), BWGEMM_VARIANT(2, 224, 6, false, 1, 2),
-    BWGEMM_VARIANT(2, 320, 5, false, 1, 1), BWGEMM_VARIANT(2, 320, 5, false, 1, 2),
+    BWGEMM_VARIANT(2, 256, 7, false, 1, 2), BWGEMM_VARIANT(1, 64, 9, true, 1, 2),
+    BWGEMM_VARIANT(2, 224, 6, false, 1, 1), BWGEMM_VARIANT(2, 224, 7, false, 1, 2),
+    BWGEMM_VARIANT(2, 320, 5, false, 1, 1), BWGEMM_VARIANT(2, 320, 6, false, 1, 2),
     BWGEMM_VARIANT(2, 384, 4, false, 1, 1),
 };
 #undef BWGEMM_VARIANT

@@ -36,9 +36,9 @@ constexpr Variant kVariants[] = {
     {1, 256, 4, false, 1, 1}, {1, 128, 6, false, 1, 1}, {2, 256, 6, false, 1, 1},
     {2, 128, 8, false, 1, 1}, {2, 128, 8, true, 1, 1},  {2, 64, 9, true, 1, 1},
     {1, 128, 6, true, 1, 1},  {1, 64, 8, true, 1, 1},   {2, 256, 6, false, 2, 1},
-    {2, 128, 8, false, 2, 1}, {2, 256, 6, false, 1, 2}, {1, 64, 8, true, 1, 2},
-    {2, 224, 6, false, 1, 1}, {2, 224, 6, false, 1, 2},
-    {2, 320, 5, false, 1, 1}, {2, 320, 5, false, 1, 2}, {2, 384, 4, false, 1, 1},
+    {2, 128, 8, false, 2, 1}, {2, 256, 7, false, 1, 2}, {1, 64, 9, true, 1, 2},
+    {2, 224, 6, false, 1, 1}, {2, 224, 7, false, 1, 2},
+    {2, 320, 5, false, 1, 1}, {2, 320, 6, false, 1, 2}, {2, 384, 4, false, 1, 1},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 

@@ -265,7 +265,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.tile_m = tile_m;
     sel.cfg.tile_n = bn;
     sel.cfg.tile_k = kTileK;
-    sel.cfg.stages = kVariants[idx].stages;
+    sel.cfg.stages = kVariants[idx_run].stages;  // the variant that runs
     sel.cfg.split_k = int32_t(s);
     sel.cfg.raster_group = int32_t(group);
     sel.cfg.num_tiles = int32_t(tiles);

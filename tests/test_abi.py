@@ -152,6 +152,8 @@ def test_select_decode_shapes():
         c = cfg(256, N, K, sms=152, pairs=76, quads=36, swap_ab=1)
         assert c["variant"] == 2 and c["tile_n"] == 256 and c["num_tiles"] == 32
         assert c["split_k"] == 2 and c["cluster_split"] == 1 and c["grid"] == 128
+        # the clustered kernel stages its output in the idle ring: seven stages
+        assert c["stages"] == 7
         # with room for 37 clusters of four the 224-wide tiles keep the cluster
         c = cfg(256, N, K, sms=152, pairs=76, quads=38, swap_ab=1)
         assert c["tile_n"] == 224 and c["num_tiles"] == 37 and c["cluster_split"] == 1
@@ -160,7 +162,7 @@ def test_select_decode_shapes():
     # 32 tiles of 320 (two MMAs per K step) x 2 slices in 32 clusters of four
     c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1)
     assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
-    assert c["cluster_split"] == 1 and c["grid"] == 128 and c["stages"] == 5
+    assert c["cluster_split"] == 1 and c["grid"] == 128 and c["stages"] == 6
     c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
     # MLP up: 112 tiles of 256 = 1.47 waves (stream-K); 75 tiles of 384 (two

@@ -634,15 +634,18 @@ __device__ __forceinline__ void pair_store(const GemmParams& p, const CUtensorMa
 // computes column block MC * n + i of the tile group (m, n); the CTAs with the
 // same rank in their pair need the same 128 A rows, so each loads 128 / MC of
 // them once from L2 and multicasts them to all MC.
-template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS, bool RS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_a2,
                 const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_c2,
                 const GemmParams p)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
+    // RS: one whole tile per CTA (a one-wave schedule), so the rings are idle
+    // when the epilogue stores and hold its output boxes
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1) || RS>;
     static_assert(MC == 1 || (MC == 2 && CG == 2), "A multicast pairs CTA pairs");
+    static_assert(!RS || (KS == 1 && MC == 1), "ring-staged output: plain whole-tile kernels only");
     static_assert(KS == 1 || (KS == 2 && MC == 1), "a cluster holds column groups or K slices");
     constexpr int CS = CG * MC * KS;  // CTAs per cluster
     // K-slice exchange: each slice sends the other the 32-column chunks it owns,
@@ -667,6 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(KS == 1 || int(kXchgBytes) <= STAGES * Cfg::kABytes, "exchange fits the A ring");
     static_assert(KS == 1 || int(kXchgBytes) + kEpiWarps * 2 * Cfg::kStoreBufBytes <= STAGES * Cfg::kBBytes,
                   "the exchange staging and the output boxes fit the B ring");
+    static_assert(!RS || kEpiWarps * 2 * Cfg::kStoreBufBytes <= STAGES * Cfg::kBBytes,
+                  "the output boxes fit the B ring");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -770,6 +775,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both CTAs' bytes of a pair are counted on the pair leader's barrier
         const uint32_t leader_full = (CG == 2) ? ptx::map_to_cta(bar_full, leader) : bar_full;
         while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusProducerTimeout)) {
+            if constexpr (RS) {
+                // a ring-staged kernel runs one unit per CTA: a second one would
+                // refill the ring its epilogue stages in -- a planning error
+                if (!first_unit) {
+                    if (lane == 0)
+                        atomicOr(p.status, kStatusBadConfig);
+                    break;
+                }
+            }
             if (first_unit) {
                 // the first unit is known; now wait for the previous kernel
                 ptx::grid_dependency_wait();
@@ -1025,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         // the clustered split stages its output boxes in the B ring after the
         // exchange block (its one unit ends with the rings idle)
-        const uint32_t store_base = (KS > 1) ? sB + kXchgBytes : sStore;
+        const uint32_t store_base = (KS > 1) ? sB + kXchgBytes : (RS ? sB : sStore);
         StoreQueue sq{store_base + uint32_t(ew * 2 * Cfg::kStoreBufBytes), 0, false};
         constexpr size_t kSlotF4 = size_t(Cfg::kPartialFloats) / 4;  // float4s per CTA partial
         float4* const parts = reinterpret_cast<float4*>(p.partials);

@@ -6,13 +6,13 @@ namespace bwgemm {
 
 namespace {
 
-template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS, bool RS>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const CUtensorMap& a2, const CUtensorMap& b2, const CUtensorMap& c2,
                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1) || RS>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS, RS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -41,11 +41,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     return cudaLaunchKernelEx(&cfg, kernel, a, b, c, a2, b2, c2, p);
 }
 
-template <int CG, int BN, int STAGES, bool TR, int MC, int KS>
+template <int CG, int BN, int STAGES, bool TR, int MC, int KS, bool RS>
 cudaError_t max_active_one(int* out)
 {
-    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1)>;
-    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS>;
+    using Cfg = KernelConfig<CG, BN, STAGES, (KS > 1) || RS>;
+    auto kernel = gemm_kernel<CG, BN, STAGES, TR, MC, KS, RS>;
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (err != cudaSuccess)
@@ -85,9 +85,10 @@ struct VariantFns {
     int smem_bytes;
 };
 
-#define BWGEMM_VARIANT(CG, BN, ST, TR, MC, KS)                                      \
-    {&launch_one<CG, BN, ST, TR, MC, KS>, &max_active_one<CG, BN, ST, TR, MC, KS>, \
-     KernelConfig<CG, BN, ST, (KS > 1)>::kSmemBytes}
+#define BWGEMM_VARIANT_RS(CG, BN, ST, TR, MC, KS, RS)                                       \
+    {&launch_one<CG, BN, ST, TR, MC, KS, RS>, &max_active_one<CG, BN, ST, TR, MC, KS, RS>, \
+     KernelConfig<CG, BN, ST, (KS > 1) || RS>::kSmemBytes}
+#define BWGEMM_VARIANT(CG, BN, ST, TR, MC, KS) BWGEMM_VARIANT_RS(CG, BN, ST, TR, MC, KS, false)
 
 // same order as kVariants in internal.h
 constexpr VariantFns kFns[] = {
@@ -100,17 +101,19 @@ constexpr VariantFns kFns[] = {
     BWGEMM_VARIANT(2, 224, 6, false, 1, 1), BWGEMM_VARIANT(2, 224, 7, false, 1, 2),
     BWGEMM_VARIANT(2, 320, 5, false, 1, 1), BWGEMM_VARIANT(2, 320, 6, false, 1, 2),
     BWGEMM_VARIANT(2, 384, 4, false, 1, 1),
+    BWGEMM_VARIANT_RS(2, 224, 7, false, 1, 1, true), BWGEMM_VARIANT_RS(2, 384, 5, false, 1, 1, true),
 };
 #undef BWGEMM_VARIANT
+#undef BWGEMM_VARIANT_RS
 static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables out of step");
 
 }  // namespace
 
-int find_variant(int cg, int bn, bool trans, int mc, int ks)
+int find_variant(int cg, int bn, bool trans, int mc, int ks, bool rs)
 {
     for (int i = 0; i < kNumVariants; ++i)
         if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans &&
-            kVariants[i].mc == mc && kVariants[i].ks == ks)
+            kVariants[i].mc == mc && kVariants[i].ks == ks && kVariants[i].rs == rs)
             return i;
     return -1;
 }

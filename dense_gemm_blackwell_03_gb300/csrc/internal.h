@@ -30,6 +30,9 @@ struct Variant {
     bool trans;  // operands swapped, accumulator holds C transposed
     int mc;      // CTA pairs per cluster sharing each A tile (1 = no multicast)
     int ks;      // K slices of a tile per cluster (1, or 2 for the clustered split-K)
+    bool rs = false;  // one whole tile per CTA: output boxes staged in the idle B ring,
+                      // whose freed room holds one more stage (the clustered split-K
+                      // variants do the same)
 };
 
 constexpr Variant kVariants[] = {
@@ -39,11 +42,12 @@ constexpr Variant kVariants[] = {
     {2, 128, 8, false, 2, 1}, {2, 256, 7, false, 1, 2}, {1, 64, 9, true, 1, 2},
     {2, 224, 6, false, 1, 1}, {2, 224, 7, false, 1, 2},
     {2, 320, 5, false, 1, 1}, {2, 320, 6, false, 1, 2}, {2, 384, 4, false, 1, 1},
+    {2, 224, 7, false, 1, 1, true}, {2, 384, 5, false, 1, 1, true},
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
 // Index into kVariants, or -1.
-int find_variant(int cg, int bn, bool trans, int mc = 1, int ks = 1);
+int find_variant(int cg, int bn, bool trans, int mc = 1, int ks = 1, bool rs = false);
 
 // Dynamic shared memory bytes of a variant.
 int variant_smem_bytes(int idx);

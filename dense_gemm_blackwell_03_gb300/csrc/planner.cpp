@@ -248,6 +248,14 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     }
     if (opts.cluster_split == 2 && !cluster_split)
         return BWGEMM_ERR_UNSUPPORTED;
+    // One whole tile per worker (every CTA's only unit): the variant that
+    // stages its output in the then idle operand ring and uses the room it
+    // saves for one more stage, where there is one.
+    if (!cluster_split && !stream_k && !clc && s == 1 && mc == 1 && tiles <= workers) {
+        const int rs_idx = find_variant(cg, bn, swap, 1, 1, true);
+        if (rs_idx >= 0)
+            idx_run = rs_idx;
+    }
     const int cs_run = cluster_split ? cg * 2 : cs;
 
     int64_t group = opts.raster_group > 0 ? opts.raster_group : 8;

@@ -169,7 +169,7 @@ def test_select_decode_shapes():
     # MMAs per K step) = one wave of whole tiles
     c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1)
     assert c["tile_n"] == 384 and c["num_tiles"] == 75 and c["split_k"] == 1
-    assert c["schedule"] == binding.SCHEDULE_TILES and c["grid"] == 150 and c["stages"] == 4
+    assert c["schedule"] == binding.SCHEDULE_TILES and c["grid"] == 150 and c["stages"] == 5
     c = cfg(256, 28672, 8192, sms=152, pairs=76, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["dp_tiles"] == 0
     # a wider tile whose split would reduce through L2 is not taken: 32 tiles
@@ -180,6 +180,10 @@ def test_select_decode_shapes():
     c = cfg(512, 8192, 5376, sms=152, pairs=76)
     assert c["schedule"] == binding.SCHEDULE_TILES and c["split_k"] == 1 and c["grid"] == 148
     assert c["tile_n"] == 224 and c["num_tiles"] == 74
+    # one tile per pair: the variant staging its output in the idle ring (7 stages);
+    # 224-wide tiles on a multi-wave shape keep the plain variant (6)
+    assert c["stages"] == 7
+    assert cfg(4096, 4096, 4096, sms=152, pairs=76, tile_n=224)["stages"] == 6
     # the width rule stays out of multi-wave, stream-K, forced and 1-SM cases
     assert cfg(4096, 4096, 4096, sms=152, pairs=76)["tile_n"] == 256
     assert cfg(8192, 28672, 8192, sms=152, pairs=76)["tile_n"] == 256

@@ -201,7 +201,14 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
  */
 bwgemm_status_t bwgemm_get_status(bwgemm_plan_t plan, void* stream);
 
-/* Raw device status bits of the last bwgemm_get_status() call (0 = fine). */
+/*
+ * Raw device status bits of the last bwgemm_get_status() call (0 = fine):
+ * 1, 2, 4, 8 = a bounded wait of the producer, the MMA warp, the epilogue or
+ * the split-K exchange ran out; 16 = a kernel variant was handed a unit it
+ * cannot run (a ring-staged or clustered split-K variant given a second or a
+ * non-split unit: a planning error, never produced by the planner).  Any bit
+ * makes bwgemm_get_status return BWGEMM_ERR_TIMEOUT.
+ */
 uint32_t bwgemm_last_device_status(bwgemm_plan_t plan);
 
 /*

@@ -23,7 +23,11 @@ measures what that step of the design is worth here:
 - Operand order for small M (C^T = B A^T).
 
 Steps fixed at compile time (128B swizzle, the ring depth, the TMEM
-double buffer) have no switch and are not timed here.  Timing: each row runs
+double buffer) have no switch and are not timed here.
+
+``python -m dense_gemm_blackwell_03_gb300.ablations --table FILE`` turns the
+JSON lines of an earlier run (FILE) into the markdown table of the timed
+rows, without a GPU.  Timing: each row runs
 about ``--warmup`` seconds, then the median of three blocks of about 0.1 s
 is taken, with CUDA events on the launching stream; inputs rotate over
 copies larger than L2.
@@ -55,6 +59,39 @@ ABLATIONS = [
 ]
 
 DEFAULT_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out", "tail_m64"]
+
+SHAPE_LABELS = {"square4096": "4096^3", "prefill_attn_out": "prefill 8192^3",
+                "decode_attn_out": "decode M=256 N=K=8192", "tail_m64": "tail M=64 N=K=8192"}
+
+
+def describe(cfg: dict) -> str:
+    """Short description of a launch configuration (the default rows' label)."""
+    parts = ["swapped" if cfg.get("swap_ab") == 1 else None,
+             "pairs" if cfg.get("variant") == 2 else "1 CTA",
+             str(cfg.get("tile_n")),
+             f"{cfg.get('copy_kblocks')} K blocks/copy" if cfg.get("copy_kblocks") == 2 else None]
+    if cfg.get("split_k", 1) > 1:
+        where = "in clusters" if cfg.get("cluster_split") == 1 else "through L2"
+        parts.append(f"split-K {cfg['split_k']} {where}")
+    else:
+        parts.append({1: "whole tiles", 2: "stream-K", 3: "cluster launch control"}.get(cfg.get("schedule"),
+                                                                                       "schedule ?"))
+    return ", ".join(p for p in parts if p)
+
+
+def markdown_table(rows) -> str:
+    """The timed rows of a run as a markdown table (untimed rows are left out)."""
+    out = ["| shape | row | us | TFLOP/s | fraction | vs default |", "|---|---|---:|---:|---:|---:|"]
+    for r in rows:
+        if "us" not in r:
+            continue
+        label = r["row"]
+        if label == "default":
+            label = f"default ({describe(r.get('config', {}))})"
+        vs = r.get("vs_default")
+        out.append(f"| {SHAPE_LABELS.get(r['shape'], r['shape'])} | {label} | {r['us']:.2f} | "
+                   f"{r['tflops']:.1f} | {r['roofline_frac']:.3f} | {'1' if vs is None else f'{vs:.3f}'} |")
+    return "\n".join(out)
 
 
 def _steady(run, sets, warmup_s):
@@ -118,7 +155,14 @@ def main(argv=None) -> int:
                          "decode attention-out, M = 64 tail)")
     ap.add_argument("--warmup", type=float, default=0.3, help="seconds of each row's own load before timing")
     ap.add_argument("--cooldown", type=float, default=0.5, help="idle seconds before each row")
+    ap.add_argument("--table", metavar="FILE",
+                    help="print the markdown table of an earlier run's JSON lines and exit (no GPU)")
     args = ap.parse_args(argv)
+    if args.table:
+        with open(args.table) as f:
+            rows = [json.loads(line) for line in f if line.startswith("{")]
+        print(markdown_table(rows))
+        return 0
     binding.load_library(build_if_missing=True)
     hbm_gbs, tflops_peak, peak_src = _peaks()
     props = torch.cuda.get_device_properties(0)

@@ -376,3 +376,27 @@ def test_plan_creation_without_gpu_fails_cleanly(lib):
     assert lib.bwgemm_destroy(None) == OK
     assert lib.bwgemm_run(None, A0, B0, C0, 1, 1, 1, 8, 8, 8, BF16, None) == INVALID
     assert lib.bwgemm_get_status(None, None) == INVALID
+
+
+@pytest.mark.parametrize("M", [1, 64, 200, 256, 512, 1024, 4096, 8192])
+@pytest.mark.parametrize("N", [1024, 5376, 8192, 10240, 28672])
+def test_one_unit_variants_get_one_unit_per_worker(M, N):
+    """The ring-staged whole-tile variants (224 with 7 stages, 384 with 5) and
+    the clustered split-K ones stage their output in the operand rings, which
+    is only safe when each worker (CTA pair, or cluster for the split) runs a
+    single unit: the planner must never hand them more (the kernels refuse a
+    second unit with a status bit)."""
+    for K in (5376, 8192):
+        for opts in ({}, {"tile_n": 224}, {"tile_n": 384}, {"schedule": binding.SCHEDULE_TILES}):
+            try:
+                c = cfg(M, N, K, sms=152, pairs=76, quads=36, **opts)
+            except binding.BwgemmError:
+                continue
+            ring_staged = c["split_k"] == 1 and c["variant"] == 2 and (
+                (c["tile_n"] == 224 and c["stages"] == 7) or (c["tile_n"] == 384 and c["stages"] == 5))
+            if ring_staged:
+                assert c["schedule"] == binding.SCHEDULE_TILES and c["sk_tiles"] == 0
+                assert c["num_units"] <= c["workers"], (M, N, K, opts, c)
+            if c["cluster_split"] == 1:
+                # one tile per cluster, one K slice per pair (or CTA) of it
+                assert c["split_k"] == 2 and c["workers"] == c["num_tiles"], (M, N, K, opts, c)

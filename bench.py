@@ -12,12 +12,15 @@ reported under "shapes".
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
-steps bracketed by a barrier and a device synchronisation on both sides.
-Inputs rotate over enough copies that their total exceeds twice the L2
-(129 MB), so no step reads operands left in L2 by the step before.  With N > 1
-(torchrun) every rank runs an independent replica ("replicas only": the GEMM
-has no exchange step), the max time over ranks is taken and `value` counts
-the work of all ranks.
+steps bracketed by a device synchronisation on both sides.  Inputs rotate
+over enough copies that their total exceeds twice the L2 (129 MB), so no step
+reads operands left in L2 by the step before.  The library runs on one GPU
+and has no multi-GPU path: ``--gpus`` other than 1 is refused.
+
+The JSON line ends with ``shapes``, a compact summary of every other page
+shape (microseconds per launch, fraction of its roofline, cuBLAS on the same
+tensors), so that it survives in a short tail of the output; the full
+per-shape records go to stderr.
 
 ``--impl reference`` times the CPU oracle (the plain fp64 triple loop) on the
 host cores on a bounded sample of the same workload.
@@ -192,16 +195,14 @@ def input_sets(shape, device, l2_bytes, max_sets=4):
     return sets
 
 
-def time_region(fn, sets, steps, warmup, stream, barrier=None):
+def time_region(fn, sets, steps, warmup, stream):
     """Run fn(A, B, C) `steps` times back to back (rotating input sets) between
-    two events on the launching stream, bracketed by a barrier and a device
-    synchronisation on both sides; return the elapsed milliseconds."""
+    two events on the launching stream, bracketed by a device synchronisation
+    on both sides; return the elapsed milliseconds."""
     import torch
     for i in range(warmup):
         fn(*sets[i % len(sets)])
     torch.cuda.synchronize()
-    if barrier:
-        barrier()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_begin.record(stream)
@@ -209,8 +210,6 @@ def time_region(fn, sets, steps, warmup, stream, barrier=None):
         fn(*sets[i % len(sets)])
     t_end.record(stream)
     torch.cuda.synchronize()
-    if barrier:
-        barrier()
     return t_begin.elapsed_time(t_end)
 
 
@@ -229,18 +228,22 @@ def time_each(fn, sets, iters, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def aggregate(local_seconds: float, work_per_step: float, steps: int, dist=None, device="cpu"):
-    """Whole-job throughput of N replicas: the max time over ranks, all ranks'
-    work.  Returns (max_seconds, work_per_second)."""
-    world = 1
-    t = local_seconds
-    if dist is not None and dist.is_initialized():
-        import torch
-        world = dist.get_world_size()
-        buf = torch.tensor([local_seconds], dtype=torch.float64, device=device)
-        dist.all_reduce(buf, op=dist.ReduceOp.MAX)
-        t = float(buf.item())
-    return t, world * work_per_step * steps / t
+def aggregate(seconds: float, work_per_step: float, steps: int):
+    """Throughput of one GPU's timed region.  Returns (seconds, work_per_second)."""
+    return seconds, work_per_step * steps / seconds
+
+
+def compact_shape(rec: dict) -> dict:
+    """The short form of one shape's record that ends the JSON line: time per
+    launch, fraction of its roofline (bound), cuBLAS's time on the same
+    tensors and the median SM clock while it ran."""
+    r = rec["roofline"]
+    out = {"us": rec["us"], "frac": r["frac"], "bound": r["bound"],
+           "cublas_us": rec.get("cublas_us")}
+    mhz = (rec.get("clocks") or {}).get("sm_mhz")
+    if mhz is not None:
+        out["mhz"] = int(mhz)
+    return out
 
 
 def roofline_entry(shape, seconds, peaks):
@@ -288,7 +291,7 @@ def cpu_baseline(shape, target_s=12.0):
 def run_reference(args):
     """--impl reference: the CPU oracle timed step by step on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if rank != 0:  # one line from rank 0 only, should a launcher start several
         return 0
     import oracle
     from dense_gemm_blackwell_03_gb300.workloads import SHAPES, bits_of, make_inputs
@@ -342,17 +345,9 @@ def run_ours(args):
     from dense_gemm_blackwell_03_gb300 import binding
     from dense_gemm_blackwell_03_gb300.workloads import SHAPES, TORCH_DTYPES, make_inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    local_rank = 0  # the one GPU this runs on
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    barrier = (lambda: dist.barrier()) if dist else None
 
     binding.load_library(build_if_missing=True)
     peaks = load_peaks()
@@ -374,7 +369,7 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)
     sampler.begin()
-    total_ms = time_region(ours, sets, args.steps, 0, stream, barrier)
+    total_ms = time_region(ours, sets, args.steps, 0, stream)
     sampler.end()
     clocks = sampler.stop()
     launches = plan.launch_count() - n0
@@ -384,7 +379,7 @@ def run_ours(args):
     kcfg = plan.last_config()
     per = time_each(ours, sets, max(50, min(args.steps, 200)), stream)
 
-    total_s, flops_per_s = aggregate(total_ms / 1e3, shape.flops, args.steps, dist, device)
+    total_s, flops_per_s = aggregate(total_ms / 1e3, shape.flops, args.steps)
     ms_per_step = total_s * 1e3 / args.steps
     value = flops_per_s / 1e12
     per_sorted = sorted(per)
@@ -406,7 +401,7 @@ def run_ours(args):
     # cuBLAS (torch.matmul) on the same tensors, as same-box context
     def cublas(A, B, C):
         torch.matmul(A, B.t(), out=C)
-    cb_ms = time_region(cublas, sets, args.steps, 5, stream, barrier)
+    cb_ms = time_region(cublas, sets, args.steps, 5, stream)
     cb_s = cb_ms / 1e3 / args.steps
 
     # end-to-end through the C ABI with host buffers (H2D of A, B and D2H of C each step)
@@ -419,12 +414,11 @@ def run_ours(args):
         for _ in range(3):
             plan.gemm_host(hA, hB, out=hC, stream=stream)
         e2e_steps = max(5, min(args.steps, 30))
-        if barrier:
-            barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             plan.gemm_host(hA, hB, out=hC, stream=stream)
-        e2e_s, e2e_flops = aggregate(time.perf_counter() - t0, shape.flops, e2e_steps, dist, device)
+        e2e_s, e2e_flops = aggregate(time.perf_counter() - t0, shape.flops, e2e_steps)
         e2e = {"value": round(e2e_flops / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": 2 * (shape.M * shape.K + shape.N * shape.K),
                "d2h_bytes_per_step": 2 * shape.M * shape.N, "steps": e2e_steps,
@@ -476,6 +470,7 @@ def run_ours(args):
                             "tflops": round(s.flops / t / 1e12, 1),
                             "gbs": round(s.algorithmic_bytes / t / 1e9, 1),
                             "roofline": r,
+                            "cublas_us": round(t_cb * 1e6, 2),
                             "cublas_tflops": round(s.flops / t_cb / 1e12, 1),
                             "kernel_config": {k: cfg[k] for k in ("variant", "tile_m", "tile_n",
                                                                   "split_k", "schedule", "grid")}}
@@ -488,13 +483,13 @@ def run_ours(args):
                                       "samples_under_load": c.get("samples_under_load", 0)}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, target_s=args.cpu_seconds)
 
     # The nominal dense peak from a measured per-SM tensor rate (a tcgen05.mma
     # probe timed in SM cycles) x SMs x the maximum SM clock; the fraction
     # against it is printed beside the one against the measured cuBLAS peak.
-    if rank == 0 and roof["bound"] == "tensor":
+    if roof["bound"] == "tensor":
         try:
             rate, sms = binding.probe_tensor_rate(local_rank)
             max_mhz = clocks.get("sm_max_mhz") if isinstance(clocks, dict) else None
@@ -504,52 +499,51 @@ def run_ours(args):
             if max_mhz:
                 peak = sms * rate * max_mhz * 1e6 / 1e12
                 nominal["peak_tflops"] = round(peak, 1)
-                nominal["frac"] = round(value / world / peak, 4)
+                nominal["frac"] = round(value / peak, 4)
         except binding.BwgemmError as e:
             nominal = {"unavailable": str(e)}
         roofline["nominal"] = nominal
 
-    if rank == 0:
-        line = {
-            "metric": METRIC,
-            "value": round(value, 2),
-            "unit": "TFLOP/s",
-            "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": round(value / world / PAGES_4096_BF16, 4),
-            "vs_baseline_ref": "1772.9 TFLOP/s bf16 4096^3 on B200 (the Blackwell deep dive's "
-                               "kernel 8); another machine's number, context only",
-            "dtype": shape.dtype,
-            "data": "synthetic: seeded N(0,1)/sqrt(K) bf16 A and B, rounded from fp32",
-            "config": {"workload": f"{shape.name}: C=A*B^T, M={shape.M} N={shape.N} K={shape.K}, "
-                                   f"{shape.dtype} in/out, fp32 accumulate",
-                       "M": shape.M, "N": shape.N, "K": shape.K,
-                       "l2": f"inputs rotate over {len(sets)} copies "
-                             f"({len(sets) * shape.algorithmic_bytes / 1e6:.0f} MB > 2x L2)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "kernel_config": kcfg},
-            "median_ms": round(median_ms, 5),
-            "p10_ms": round(per_sorted[len(per) // 10], 5),
-            "p90_ms": round(per_sorted[(9 * len(per)) // 10], 5),
-            "per_iteration_note": f"median/p10/p90 over {len(per)} separately event-timed iterations",
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "cublas_tflops": round(shape.flops / cb_s / 1e12, 1),
-            "peaks": peaks,
-            "shapes": shapes,
-        }
-        print(json.dumps(line), flush=True)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / PAGES_4096_BF16, 4),
+        "vs_baseline_ref": "1772.9 TFLOP/s bf16 4096^3 on B200 (the Blackwell deep dive's "
+                           "kernel 8); another machine's number, context only",
+        "dtype": shape.dtype,
+        "data": "synthetic: seeded N(0,1)/sqrt(K) bf16 A and B, rounded from fp32",
+        "config": {"workload": f"{shape.name}: C=A*B^T, M={shape.M} N={shape.N} K={shape.K}, "
+                               f"{shape.dtype} in/out, fp32 accumulate",
+                   "M": shape.M, "N": shape.N, "K": shape.K,
+                   "l2": f"inputs rotate over {len(sets)} copies "
+                         f"({len(sets) * shape.algorithmic_bytes / 1e6:.0f} MB > 2x L2)",
+                   "parallelism": "single GPU",
+                   "kernel_config": kcfg},
+        "median_ms": round(median_ms, 5),
+        "p10_ms": round(per_sorted[len(per) // 10], 5),
+        "p90_ms": round(per_sorted[(9 * len(per)) // 10], 5),
+        "per_iteration_note": f"median/p10/p90 over {len(per)} separately event-timed iterations",
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "cublas_tflops": round(shape.flops / cb_s / 1e12, 1),
+        "peaks": peaks,
+    }
+    if shapes:
+        # full per-shape records to stderr; the compact summary ends the line
+        log(json.dumps({"shapes_detail": shapes}))
+    line["shapes"] = {name: compact_shape(rec) for name, rec in shapes.items()}
+    print(json.dumps(line, separators=(",", ":")), flush=True)
     plan.close()
-    if dist:
-        dist.barrier()
-        dist.destroy_process_group()
     return 0
 
 
@@ -575,6 +569,11 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.gpus != 1:
+        # one GPU only: the GEMM has no multi-GPU path (no sharding, no replicas)
+        print(f"bench.py: --gpus {args.gpus} refused: bwgemm runs on one GPU (use --gpus 1)",
+              file=sys.stderr, flush=True)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -37,7 +37,7 @@ EXPORTED = [
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
     "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
     "bwgemm_plan_read_trace", "bwgemm_tune", "bwgemm_plan_tuned_count",
-    "bwgemm_probe_tensor_rate",
+    "bwgemm_probe_tensor_rate", "bwgemm_noalloc_scratch",
 ]
 
 # timeline slots of bwgemm_plan_read_trace
@@ -145,6 +145,10 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_run_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                                   ctypes.c_int, i32, vp]
         lib.bwgemm_run_splitk_noalloc.restype = st
+        lib.bwgemm_noalloc_scratch.argtypes = [i32, i32, i64, i64, i64, i32,
+                                               ctypes.POINTER(ctypes.c_uint64),
+                                               ctypes.POINTER(ctypes.c_uint64)]
+        lib.bwgemm_noalloc_scratch.restype = st
         lib.bwgemm_get_status.argtypes = [vp, vp]
         lib.bwgemm_get_status.restype = st
         lib.bwgemm_last_device_status.argtypes = [vp]
@@ -269,6 +273,13 @@ class Plan:
     def __exit__(self, *exc):
         self.close()
 
+    def _check_device(self, *tensors):
+        # the library refuses operands that are not memory of the plan's
+        # device as well; this names the tensor
+        for name, t in zip(("A", "B", "out"), tensors):
+            if t.device.type != "cuda" or t.device.index != self.device:
+                raise ValueError(f"{name} is on {t.device}, the plan on cuda:{self.device}")
+
     @staticmethod
     def _stream_handle(stream):
         import torch
@@ -298,6 +309,7 @@ class Plan:
             out = torch.empty((M, N), dtype=A.dtype, device=A.device)
         elif out.dtype != A.dtype or tuple(out.shape) != (M, N) or not out.is_cuda:
             raise ValueError("out must be an M x N CUDA tensor of the operands' dtype")
+        self._check_device(A, B, out)
         rc = self.lib.bwgemm_run(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
                                  _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream))
         if rc != 0:
@@ -347,6 +359,7 @@ class Plan:
         N, _ = B.shape
         if out is None:
             out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+        self._check_device(A, B, out)
         cfg = Config()
         rc = self.lib.bwgemm_tune(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
                                   _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream), int(iters),

@@ -184,6 +184,25 @@ struct DeviceGuard {
 
 }  // namespace
 
+namespace bwgemm {
+
+bwgemm_status_t check_operands_resident(const void* A, const void* B, const void* C, int64_t K, int device)
+{
+    const void* ptrs[3] = {C, A, B};
+    for (int i = 0; i < (K > 0 ? 3 : 1); ++i) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();  // an address the driver does not know: not this GPU's memory
+            return BWGEMM_ERR_INVALID_ARG;
+        }
+        if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != device)
+            return BWGEMM_ERR_INVALID_ARG;
+    }
+    return BWGEMM_OK;
+}
+
+}  // namespace bwgemm
+
 struct bwgemm_plan_s {
     int device = 0;
     int num_sms = 0;
@@ -239,6 +258,10 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, c
         return st;
     if (M == 0 || N == 0)
         return BWGEMM_OK;
+    // operands on another GPU or in host memory are refused before any tensor
+    // map is encoded on them
+    if ((st = check_operands_resident(A, B, C, K, plan->device)) != BWGEMM_OK)
+        return st;
     if (K == 0) {  // empty sum: C = 0
         if (cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream) != cudaSuccess)
             return BWGEMM_ERR_CUDA;

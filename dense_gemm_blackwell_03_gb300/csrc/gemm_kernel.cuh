@@ -81,8 +81,8 @@ struct KernelConfig {
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kOffBar = kOffStore + (RING_STORE ? 0 : kEpiWarps * 2 * kStoreBufBytes);
     // full[S], empty[S], acc_full[2], acc_empty[2], clc_full[4], clc_empty[4],
-    // exchange_ready, exchange_full[2], exchange_staged[2]
-    static constexpr int kNumBars = 2 * STAGES + 9 + 2 * kClcSlots;
+    // exchange_ready, exchange_full[2], exchange_staged[2], mma_drain
+    static constexpr int kNumBars = 2 * STAGES + 10 + 2 * kClcSlots;
     // 16-byte responses on 16-byte boundaries (the barrier count may be odd)
     static constexpr int kOffClcResp = (kOffBar + kNumBars * 8 + 15) & ~15;
     static constexpr int kOffTmemSlot = kOffClcResp + 16 * kClcSlots;
@@ -427,6 +427,36 @@ __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint3
     }
 }
 
+// After an abort: wait, bounded by `limit_ns` alone (the abort flag is
+// already set), until the phase of `bar` with `parity` completed.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    WaitClock clock;
+#pragma unroll 1
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (clock.expired(limit_ns))
+            return false;
+    return true;
+}
+
+// After an abort: let `ns` of %globaltimer pass (bounded by polls too, should
+// the timer stop), so that copies whose completion this CTA cannot observe --
+// a pair follower's loads, counted on the leader's barriers; multicast loads
+// from the other pair; an exchange copy in flight to or from the partner --
+// land before the cluster's shared memory is released.
+__device__ __noinline__ void settle(uint64_t ns)
+{
+    WaitClock clock;
+#pragma unroll 1
+    while (!clock.expired(ns)) {
+    }
+}
+
+// Bounds of the abort drain: ample for any copy or MMA in flight (they take
+// microseconds), and short beside the wait limit that caused the abort.
+constexpr uint64_t kDrainNs = 2000000;  // per drained barrier
+constexpr uint64_t kSettleNs = 50000;
+
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi, int dtype)
 {
     const float a = __uint_as_float(lo), b = __uint_as_float(hi);
@@ -698,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_xready = bar_clc_empty + 8 * kClcSlots;    // the other slice's ring is free
     const uint32_t bar_xfull = bar_xready + 8;      // + 8 * half: the other slice's chunks landed
     const uint32_t bar_xstaged = bar_xfull + 16;    // + 8 * half: the half's four warps staged their rows
+    const uint32_t bar_drain = bar_xstaged + 16;    // after an abort: the issued MMAs completed
     const uint32_t clc_resp = base + Cfg::kOffClcResp;     // + 16 * slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
@@ -722,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar_xfull + 8 * h, 1);  // own arrive.expect_tx; the partner's bulk-copy bytes
             ptx::mbar_init(bar_xstaged + 8 * h, kEpiWarps / 2);
         }
+        ptx::mbar_init(bar_drain, 1);  // one tcgen05.commit
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -755,6 +787,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scheduled from here on.
     ptx::launch_dependents();
     const uint32_t clc_empty_leader = (CS > 1) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
+    // producer (warp 0) of a CTA whose full barriers count its loads (one CTA,
+    // or a pair leader): stages armed with a load, and the parity of the phase
+    // each last armed fill completes -- what the abort drain waits for
+    uint32_t armed_mask = 0, armed_parity = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -864,6 +900,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rel = kb - w.kb0;
                 const bool stall = p.stall_kblock >= 0 && blockIdx.x == 0 && first_unit &&
                                    p.stall_kblock >= rel && p.stall_kblock < rel + nkb;
+                if (!stall && (CG == 1 || prank == 0)) {  // warp-uniform bookkeeping
+                    armed_mask |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                }
                 if (!stall && ptx::elect_one()) {
                     if (first_unit && kb == w.kb0)
                         trace_mark(p, kTraceFirstLoad);
@@ -1492,7 +1532,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // --------------------------------------------------------------- teardown
+    // Every role of this CTA has left its loop, so the abort flag is final.
+    // After an abort, asynchronous work may still be in flight: drain it
+    // (bounded) before the CTA's shared memory and TMEM are released.  The
+    // MMA thread commits once more and waits, so every MMA it issued has
+    // completed; the producer waits for each stage it armed to land; then the
+    // CTA settles for copies it cannot observe.  Without an abort none of
+    // this runs (every load was consumed, every MMA committed and waited for
+    // by the epilogue, every store waited for above).
     __syncwarp();
+    __syncthreads();
+    if (*abort_flag) {
+        if (warp == 1 && prank == 0) {
+            if (ptx::elect_one()) {  // the lane that issued the MMAs
+                if constexpr (CG == 1)
+                    ptx::mma_commit(bar_drain);
+                else
+                    ptx::mma_commit_pair(bar_drain, uint16_t(1u << rank));
+            }
+            __syncwarp();
+            drain_wait(bar_drain, 0u, kDrainNs);
+        }
+        if (warp == 0) {
+#pragma unroll 1
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed_mask >> s) & 1u)
+                    drain_wait(bar_full + 8 * s, (armed_parity >> s) & 1u, kDrainNs);
+            if (lane == 0)
+                settle(kSettleNs);
+        }
+        __syncwarp();
+        __syncthreads();
+    }
     ptx::tc_fence_before_sync();
     if constexpr (CS > 1)
         ptx::cluster_sync();

@@ -72,6 +72,13 @@ cudaError_t variant_max_active(int idx, int* out);
 constexpr int kHostChunksMax = 8;
 int64_t host_block_rows(int64_t M, int64_t N, int64_t K);
 
+// BWGEMM_OK when every operand a call reads or writes (A and B only when
+// K > 0) is device or managed memory of `device`; BWGEMM_ERR_INVALID_ARG
+// otherwise (host memory, memory of another GPU, an address the driver does
+// not know).  Tensor maps, plain or multicast, are then only ever encoded on
+// this GPU's own memory.
+bwgemm_status_t check_operands_resident(const void* A, const void* B, const void* C, int64_t K, int device);
+
 // Sizes of the split-K workspace regions.
 constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) arrival counters
 

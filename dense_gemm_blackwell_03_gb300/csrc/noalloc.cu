@@ -23,11 +23,14 @@ namespace {
 
 using namespace bwgemm;
 
-constexpr size_t kNoAllocPartialBytes = size_t(8) << 20;  // fp32 partial tiles
-constexpr size_t kNoAllocCounters = 16384;                // per (tile, cta, warp) counters
-constexpr size_t kNoAllocCounterBytes = kNoAllocCounters * sizeof(uint32_t);
+constexpr size_t kNoAllocPartialBytes = BWGEMM_NOALLOC_PARTIAL_BYTES;  // fp32 partial tiles
+constexpr size_t kNoAllocCounterBytes = BWGEMM_NOALLOC_COUNTER_BYTES;  // per (tile, cta, warp) counters
+constexpr size_t kNoAllocCounters = kNoAllocCounterBytes / sizeof(uint32_t);
 constexpr size_t kNoAllocStatusBytes = 256;
 constexpr size_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocCounterBytes + kNoAllocStatusBytes;
+static_assert(kNoAllocCounters * sizeof(uint32_t) == kNoAllocCounterBytes, "whole counters");
+static_assert(kNoAllocPartialBytes % 256 == 0 && kNoAllocCounterBytes % 256 == 0,
+              "the counter region and the status word stay 256-byte aligned");
 
 // layout: [partials 8 MiB][counters 64 KiB][status word (+ pad)]
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -74,6 +77,36 @@ bool encode(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype, int
     return enc(map, dtype == BWGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The plan of an allocation-free call and the scratch it uses: split-K over
+// whole tiles with the operands in the order given, one CTA pair (or CTA) per
+// cluster, slices reducing through the array.  Host only.  When the planner
+// cuts the split to one slice (K of one 64-wide block) no partials or
+// counters are used, and the counters of the call are not touched.
+bwgemm_status_t noalloc_select(int num_sms, int max_pairs, int64_t M, int64_t N, int64_t K, int32_t split_k,
+                               Selection* sel, size_t* partial_bytes, size_t* counters)
+{
+    if (split_k < 2 || split_k > 16)
+        return BWGEMM_ERR_INVALID_ARG;
+    bwgemm_plan_options_t opts;
+    bwgemm_default_options(&opts);
+    opts.split_k = split_k;
+    opts.swap_ab = 1;        // operands in the order given
+    opts.multicast = 1;      // one CTA pair per cluster: the scratch below is sized for it
+    opts.cluster_split = 1;  // slices reduce through the scratch array, not in a cluster
+    // plan as if the workspace were unbounded, then hold the need against the array
+    const bwgemm_status_t st = select_config(num_sms, max_pairs, 0, M, N, K, opts, ~uint64_t(0), sel);
+    if (st != BWGEMM_OK)
+        return st;
+    const Variant& v = kVariants[sel->variant_idx];
+    const bool split = sel->cfg.split_k > 1;
+    const size_t tiles = size_t(sel->cfg.num_tiles);
+    *partial_bytes = split ? tiles * size_t(sel->cfg.split_k) * size_t(v.cg) * kRowsPerCta * size_t(v.bn) * 4 : 0;
+    *counters = split ? tiles * size_t(v.cg) * kEpiWarps * kCountersPerWarp : 0;
+    if (*partial_bytes > kNoAllocPartialBytes || *counters > kNoAllocCounters)
+        return BWGEMM_ERR_WORKSPACE;  // this shape's split-K scratch exceeds the fixed array
+    return BWGEMM_OK;
 }
 
 // Once per device, with that device current: resolve the array's device
@@ -127,14 +160,18 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0)
         return BWGEMM_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return BWGEMM_ERR_NO_DEVICE;
+    // the operands must be memory of the current device (no tensor map is
+    // encoded on another GPU's or on host memory)
+    if ((st = check_operands_resident(A, B, C, K, dev)) != BWGEMM_OK)
+        return st;
     if (K == 0)  // empty sum: C = 0
         return cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), s) == cudaSuccess
                    ? BWGEMM_OK
                    : BWGEMM_ERR_CUDA;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return BWGEMM_ERR_NO_DEVICE;
     DeviceSetup* ds = nullptr;
     if ((st = setup_device(dev, &ds)) != BWGEMM_OK)
         return st;
@@ -142,31 +179,19 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     if (!enc)
         return BWGEMM_ERR_NO_DEVICE;
 
-    bwgemm_plan_options_t opts;
-    bwgemm_default_options(&opts);
-    opts.split_k = split_k;
-    opts.swap_ab = 1;    // operands in the order given
-    opts.multicast = 1;      // one CTA pair per cluster: the scratch below is sized for it
-    opts.cluster_split = 1;  // slices reduce through the scratch array, not in a cluster
     Selection sel;
-    // plan as if the workspace were unbounded, then hold the need against the array
-    if ((st = select_config(ds->num_sms, ds->max_pairs, 0, M, N, K, opts, ~uint64_t(0), &sel)) !=
+    size_t partial_bytes = 0, counters = 0;  // used regions of the array
+    if ((st = noalloc_select(ds->num_sms, ds->max_pairs, M, N, K, split_k, &sel, &partial_bytes, &counters)) !=
         BWGEMM_OK)
         return st;
     const Variant& v = kVariants[sel.variant_idx];
-    const int S = sel.cfg.split_k;
-    const size_t tiles = size_t(sel.cfg.num_tiles);
-    const size_t partial_bytes = tiles * size_t(S) * size_t(v.cg) * kRowsPerCta * size_t(v.bn) * 4;
-    const size_t counters = tiles * size_t(v.cg) * kEpiWarps * kCountersPerWarp;
-    if (S > 1 && (partial_bytes > kNoAllocPartialBytes || counters > kNoAllocCounters))
-        return BWGEMM_ERR_WORKSPACE;  // this shape's split-K scratch exceeds the fixed array
 
     unsigned char* partials = ds->scratch;
     uint32_t* ctr = reinterpret_cast<uint32_t*>(ds->scratch + kNoAllocPartialBytes);
     uint32_t* status = reinterpret_cast<uint32_t*>(ds->scratch + kNoAllocPartialBytes + kNoAllocCounterBytes);
-    // the array keeps the previous call's contents: the arrival counters and the
-    // status word must start at zero
-    if (cudaMemsetAsync(ctr, 0, counters * sizeof(uint32_t), s) != cudaSuccess ||
+    // the array keeps the previous call's contents: the arrival counters this
+    // call uses (none without a split) and the status word must start at zero
+    if ((counters > 0 && cudaMemsetAsync(ctr, 0, counters * sizeof(uint32_t), s) != cudaSuccess) ||
         cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess)
         return BWGEMM_ERR_CUDA;
 
@@ -192,4 +217,26 @@ extern "C" bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* 
     return launch_variant(sel.variant_idx, ta, tb, tc, ta, tb, tc, p, sel.cfg.grid, s, false) == cudaSuccess
                ? BWGEMM_OK
                : BWGEMM_ERR_CUDA;
+}
+
+extern "C" bwgemm_status_t bwgemm_noalloc_scratch(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
+                                                  int64_t K, int32_t split_k, uint64_t* partial_bytes,
+                                                  uint64_t* counter_bytes)
+{
+    if (!partial_bytes || !counter_bytes || num_sms <= 0 || M < 0 || N < 0 || K < 0)
+        return BWGEMM_ERR_INVALID_ARG;
+    *partial_bytes = 0;
+    *counter_bytes = 0;
+    if (split_k < 2 || split_k > 16)
+        return BWGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || K == 0)
+        return BWGEMM_OK;  // no kernel: nothing of the array is used
+    Selection sel;
+    size_t parts = 0, counters = 0;
+    const bwgemm_status_t st = noalloc_select(num_sms, max_pairs, M, N, K, split_k, &sel, &parts, &counters);
+    if (st == BWGEMM_OK || st == BWGEMM_ERR_WORKSPACE) {
+        *partial_bytes = parts;
+        *counter_bytes = counters * sizeof(uint32_t);
+    }
+    return st;
 }

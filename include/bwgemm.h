@@ -40,6 +40,10 @@ extern "C" {
 #define BWGEMM_VERSION_MAJOR 0
 #define BWGEMM_VERSION_MINOR 2
 
+/* Regions of the fixed device array behind bwgemm_run_splitk_noalloc. */
+#define BWGEMM_NOALLOC_PARTIAL_BYTES (8u << 20) /* fp32 partial tiles of the K slices */
+#define BWGEMM_NOALLOC_COUNTER_BYTES (64u << 10) /* 32-bit arrival counters           */
+
 typedef struct bwgemm_plan_s* bwgemm_plan_t;
 
 typedef enum {
@@ -171,8 +175,11 @@ bwgemm_status_t bwgemm_destroy(bwgemm_plan_t plan);
  *   B : device pointer, N x K, row stride ldb (read only; may alias A)
  *   C : device pointer, M x N, row stride ldc (written; must not overlap A or B)
  *
- * The caller owns A, B and C and keeps them alive until the stream reaches
- * the launch.  Asynchronous: returns after enqueueing one kernel (none when
+ * A, B and C must be device (or managed) memory of the plan's device: an
+ * operand in host memory or on another GPU is refused with
+ * BWGEMM_ERR_INVALID_ARG before anything is encoded or launched (A and B are
+ * not checked when K == 0).  The caller owns A, B and C and keeps them alive
+ * until the stream reaches the launch.  Asynchronous: returns after enqueueing one kernel (none when
  * M == 0 or N == 0; a zero fill of C when K == 0, the empty sum).  No host
  * synchronisation and no device allocation, so it may be captured in a CUDA
  * graph.  Argument errors are returned synchronously and launch nothing.
@@ -299,15 +306,19 @@ int32_t bwgemm_plan_tuned_count(bwgemm_plan_t plan);
  * device-wide synchronisation cudaMalloc / cudaFree can cause -- and so
  * cannot create a plan.  Needs no plan: the split-K scratch (fp32 partial
  * tiles, arrival counters, a status word) lives in one fixed device array of
- * 8 MiB + 64 KiB + 256 B inside the library, present on every GPU that loads
- * it until the process exits.
+ * BWGEMM_NOALLOC_PARTIAL_BYTES + BWGEMM_NOALLOC_COUNTER_BYTES + 256 B inside
+ * the library, present on every GPU that loads it until the process exits.
  *
  *   A, B, C, M, N, K, lda, ldb, ldc, dtype : as for bwgemm_run (caller-owned
- *          device pointers; same alignment rules and error codes)
+ *          pointers, device or managed memory of the current device; same
+ *          alignment rules and error codes)
  *   split_k : K slices per output tile, 2..16 (capped at the number of
- *          64-wide K blocks); the partial tiles of all slices must fit the
- *          8 MiB array (tiles x split_k x 128 KiB for the 256-column tiles),
+ *          64-wide K blocks; with one K block the call runs unsplit and uses
+ *          no partials or counters); the partial tiles of all slices must
+ *          fit the partial region (tiles x split_k x 128 KiB for the
+ *          256-column tiles) and their arrival counters the counter region,
  *          else BWGEMM_ERR_WORKSPACE is returned and nothing is launched
+ *          (bwgemm_noalloc_scratch answers this on the host beforehand)
  *   stream : cudaStream_t (NULL = legacy default stream)
  *
  * The first call on a device (with that device current) resolves the
@@ -323,6 +334,21 @@ bwgemm_status_t bwgemm_run_splitk_noalloc(const void* A, const void* B, void* C,
                                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                           int64_t ldc, bwgemm_dtype_t dtype, int32_t split_k,
                                           void* stream);
+
+/*
+ * Host-only (no device access): the parts of the fixed array that
+ * bwgemm_run_splitk_noalloc would use for these sizes on a GPU with
+ * `num_sms` SMs holding `max_pairs` co-resident CTA pairs (0 = num_sms / 2).
+ * *partial_bytes and *counter_bytes receive the bytes of the partial-tile
+ * and counter regions the call writes (both 0 when it runs unsplit or
+ * launches nothing).  Returns BWGEMM_ERR_WORKSPACE (the sizes still filled
+ * in) when they exceed BWGEMM_NOALLOC_PARTIAL_BYTES or
+ * BWGEMM_NOALLOC_COUNTER_BYTES, BWGEMM_ERR_INVALID_ARG for a NULL output,
+ * negative sizes or split_k outside 2..16.
+ */
+bwgemm_status_t bwgemm_noalloc_scratch(int32_t num_sms, int32_t max_pairs, int64_t M, int64_t N,
+                                       int64_t K, int32_t split_k, uint64_t* partial_bytes,
+                                       uint64_t* counter_bytes);
 
 /* Static text for a status code ("unknown status" for anything else). */
 const char* bwgemm_status_string(bwgemm_status_t status);

@@ -400,3 +400,39 @@ def test_one_unit_variants_get_one_unit_per_worker(M, N):
             if c["cluster_split"] == 1:
                 # one tile per cluster, one K slice per pair (or CTA) of it
                 assert c["split_k"] == 2 and c["workers"] == c["num_tiles"], (M, N, K, opts, c)
+
+
+def test_noalloc_scratch_stays_inside_the_array(lib):
+    """The allocation-free entry point's use of its fixed array, on the host:
+    a split cut to one slice writes no counters or partials, every accepted
+    call fits both regions, and shapes that do not fit are refused."""
+    PART, CTRS = 8 << 20, 64 << 10
+    p, c = ctypes.c_uint64(), ctypes.c_uint64()
+
+    def need(M, N, K, S, sms=148, pairs=74):
+        rc = lib.bwgemm_noalloc_scratch(sms, pairs, M, N, K, S, ctypes.byref(p), ctypes.byref(c))
+        return rc, p.value, c.value
+
+    # K of one 64-wide block: the split is cut to one slice, nothing is cleared
+    # (before, this cleared 256 KiB of counters for 4096 tiles into a 64 KiB region)
+    assert need(16384, 16384, 64, 2) == (OK, 0, 0)
+    assert need(256, 512, 64, 4) == (OK, 0, 0)
+    # two K blocks: the same tiles now need partials and counters beyond the array
+    rc, parts, ctrs = need(16384, 16384, 128, 2)
+    assert rc == WORKSPACE and parts > PART and ctrs > CTRS
+    # 2 pair tiles x 3 slices x 2 CTAs x 128 x 256 fp32; 2 tiles x 2 CTAs x 8 warps counters
+    assert need(256, 512, 1600, 3) == (OK, 2 * 3 * 2 * 128 * 256 * 4, 2 * 2 * 8 * 4)
+    assert need(0, 512, 1600, 3) == (OK, 0, 0) and need(256, 512, 0, 3) == (OK, 0, 0)
+    for M in (1, 100, 256, 300, 1000, 4096):
+        for N in (64, 264, 1024, 8192):
+            for K in (16, 64, 65, 1000, 8192):
+                for S in (2, 3, 8, 16):
+                    rc, parts, ctrs = need(M, N, K, S)
+                    assert rc in (OK, WORKSPACE), (M, N, K, S, rc)
+                    if rc == OK:
+                        assert parts <= PART and ctrs <= CTRS, (M, N, K, S, parts, ctrs)
+                    if K <= 64:
+                        assert (parts, ctrs) == (0, 0), (M, N, K, S)
+    assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 1, ctypes.byref(p), ctypes.byref(c)) == INVALID
+    assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 17, ctypes.byref(p), ctypes.byref(c)) == INVALID
+    assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 2, None, ctypes.byref(c)) == INVALID

@@ -515,6 +515,28 @@ def test_rejects_misaligned_on_device(plan):
     assert e.value.status == 2
 
 
+def test_rejects_operands_not_on_the_plan_device(plan):
+    # pinned host memory is device-accessible, but no tensor map may cover
+    # anything but this GPU's own memory: bwgemm_run refuses before encoding
+    A = make_matrix(256, 512, "int2", seed=940, device="cuda")
+    C = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+    hA = torch.zeros(256, 512, dtype=torch.bfloat16).pin_memory()
+    hC = torch.zeros(256, 256, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream().cuda_stream
+    n_before = plan.launch_count()
+    for a, b, c in ((hA, A, C), (A, hA, C), (A, A, hC)):
+        rc = plan.run_raw(a.data_ptr(), b.data_ptr(), c.data_ptr(), 256, 256, 512, 512, 512, 256,
+                          binding.BF16, stream)
+        assert rc == 1  # BWGEMM_ERR_INVALID_ARG
+    assert plan.launch_count() == n_before
+    with pytest.raises(ValueError):
+        plan.gemm(A, hA)  # the binding names the tensor first
+    # device memory of this GPU is accepted, and the product is right
+    C = plan.gemm(A, A, out=C)
+    assert plan.status() == 0
+    compare(bits_of(C), oracle.gemm(bits_of(A), bits_of(A), "bf16"), "bf16", 512, exact=True)
+
+
 def test_host_buffers_round_trip(plan):
     A = make_matrix(300, 264, "int2", seed=930)
     B = make_matrix(200, 264, "int2", seed=931)

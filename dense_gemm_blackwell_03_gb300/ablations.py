@@ -23,7 +23,18 @@ measures what that step of the design is worth here:
 - Operand order for small M (C^T = B A^T).
 
 Steps fixed at compile time (128B swizzle, the ring depth, the TMEM
-double buffer) have no switch and are not timed here.
+double buffer) have no switch in the GEMM.  Two microbenchmarks cover the
+measurements the CuTeDSL post makes of them instead:
+
+- ``--load-path``: the load path in isolation, no MMA
+  (``bwgemm_bench_load_path``): the GEMM's ring filled by TMA and freed as
+  each stage lands, with the 128B swizzle, without it (the same copies,
+  plain rows), and in the tensor cores' unswizzled interleaved layout; the
+  post's step 4 measured 3.85 TB/s without and 18.5 TB/s with the swizzle on
+  B200.
+- ``--epilogue-share``: the epilogue's share of an unmodified launch, from
+  the kernel's own per-unit timestamps (the post's step 5: at most 13 of
+  109 us at 4096^3 on B200).
 
 ``python -m dense_gemm_blackwell_03_gb300.ablations --table FILE`` turns the
 JSON lines of an earlier run (FILE) into the markdown table of the timed
@@ -94,6 +105,80 @@ def markdown_table(rows) -> str:
     return "\n".join(out)
 
 
+# the CuTeDSL post's figures (B200), quoted beside the GB300 rows
+PAGE_LOAD_PATH_TBS = {0: 18.5, 1: 3.85}
+LOAD_PATH_STAGES = 6
+LOAD_PATH_KBLOCKS = 4096
+EPILOGUE_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out"]
+
+
+def load_path_table(rows) -> str:
+    """Markdown table of --load-path rows."""
+    out = ["| layout | copies per 32 KiB stage | TB/s (GB300) | vs 128B swizzle | post, B200 (TB/s) |",
+           "|---|---:|---:|---:|---:|"]
+    for r in rows:
+        page = PAGE_LOAD_PATH_TBS.get(r["layout"])
+        out.append(f"| {r['row']} | {r['copies_per_stage']} | {r['gbs'] / 1e3:.2f} | "
+                   f"{r['vs_swizzle']:.3f} | {'' if page is None else page} |")
+    return "\n".join(out)
+
+
+def epilogue_table(rows) -> str:
+    """Markdown table of --epilogue-share rows."""
+    out = ["| shape | span (us) | units per CTA | epilogue busy per CTA (us) | busy share | "
+           "exposed after last MMA (us) | exposed share |",
+           "|---|---:|---:|---:|---:|---:|---:|"]
+    for r in rows:
+        e = r["epilogue"]
+        out.append(f"| {SHAPE_LABELS.get(r['shape'], r['shape'])} | {e['span_us']:.2f} | "
+                   f"{r['units_per_cta']:.2f} | {e['busy_us_per_cta']:.2f} | {e['busy_share']:.3f} | "
+                   f"{e['exposed_us']:.2f} | {e['exposed_share']:.3f} |")
+    return "\n".join(out)
+
+
+def run_load_path(device: int = 0):
+    """The three layouts of bwgemm_bench_load_path, as JSON rows."""
+    from . import binding
+    rows = []
+    for layout in (0, 1, 2):
+        gbs, ms = binding.bench_load_path(layout, 0, 0, LOAD_PATH_STAGES, LOAD_PATH_KBLOCKS, device)
+        rows.append({"kind": "load_path", "layout": layout, "row": binding.LOAD_PATH_LAYOUTS[layout],
+                     "copies_per_stage": 16 if layout == 2 else 2, "stages": LOAD_PATH_STAGES,
+                     "kblocks_per_cta": LOAD_PATH_KBLOCKS, "gbs": round(gbs, 1), "ms": round(ms, 4)})
+    for r in rows:
+        r["vs_swizzle"] = round(r["gbs"] / rows[0]["gbs"], 4)
+    return rows
+
+
+def run_epilogue_share(names, warmup: int = 6):
+    """One traced launch of each named shape (default plan, after warm-up
+    launches on rotating inputs): the epilogue's share, as JSON rows."""
+    import torch
+
+    from . import binding, timeline
+    from .workloads import SHAPES, make_inputs
+    rows = []
+    for name in names:
+        s = SHAPES[name]
+        sets = [make_inputs(s, device="cuda", seed=100 + i) for i in range(3)]
+        with binding.Plan(0, trace=1) as plan:
+            for i in range(warmup):
+                plan.gemm(*sets[i % 3])
+            torch.cuda.synchronize()
+            plan.gemm(*sets[0])
+            if plan.status() != 0:
+                raise SystemExit(f"device status error on {name}")
+            trace = plan.read_trace()
+            cfg = plan.last_config()
+        per = timeline.units(trace)
+        rows.append({"kind": "epilogue_share", "shape": name, "epilogue": timeline.epilogue_share(trace),
+                     "units_per_cta": round(sum(len(u) for u in per) / max(1, len(per)), 3),
+                     "config": {k: cfg[k] for k in ("variant", "tile_n", "split_k", "schedule", "grid")}})
+        del sets
+        torch.cuda.empty_cache()
+    return rows
+
+
 def _steady(run, sets, warmup_s):
     """Seconds per launch in steady state (CUDA events, median of 3 blocks)."""
     import torch
@@ -157,13 +242,35 @@ def main(argv=None) -> int:
     ap.add_argument("--cooldown", type=float, default=0.5, help="idle seconds before each row")
     ap.add_argument("--table", metavar="FILE",
                     help="print the markdown table of an earlier run's JSON lines and exit (no GPU)")
+    ap.add_argument("--load-path", action="store_true",
+                    help="also run the load-path microbenchmark (no MMA; three layouts)")
+    ap.add_argument("--epilogue-share", action="store_true",
+                    help="also measure the epilogue's share of one traced launch per shape")
+    ap.add_argument("--only-microbench", action="store_true",
+                    help="run only the microbenchmarks asked for, not the plan-option rows")
     args = ap.parse_args(argv)
     if args.table:
         with open(args.table) as f:
             rows = [json.loads(line) for line in f if line.startswith("{")]
-        print(markdown_table(rows))
+        gemm_rows = [r for r in rows if r.get("kind") is None]
+        if gemm_rows:
+            print(markdown_table(gemm_rows))
+        lp = [r for r in rows if r.get("kind") == "load_path"]
+        if lp:
+            print("\n" + load_path_table(lp))
+        ep = [r for r in rows if r.get("kind") == "epilogue_share"]
+        if ep:
+            print("\n" + epilogue_table(ep))
         return 0
     binding.load_library(build_if_missing=True)
+    if args.load_path:
+        for row in run_load_path():
+            print(json.dumps(row), flush=True)
+    if args.epilogue_share:
+        for row in run_epilogue_share(args.shape or EPILOGUE_SHAPES):
+            print(json.dumps(row), flush=True)
+    if args.only_microbench:
+        return 0
     hbm_gbs, tflops_peak, peak_src = _peaks()
     props = torch.cuda.get_device_properties(0)
     l2_bytes = int(getattr(props, "L2_cache_size", 129 * 10 ** 6)) or 129 * 10 ** 6

@@ -37,8 +37,12 @@ EXPORTED = [
     "bwgemm_select_config", "bwgemm_plan_last_config", "bwgemm_plan_launch_count",
     "bwgemm_status_string", "bwgemm_version", "bwgemm_run_splitk_noalloc",
     "bwgemm_plan_read_trace", "bwgemm_tune", "bwgemm_plan_tuned_count",
-    "bwgemm_probe_tensor_rate", "bwgemm_noalloc_scratch",
+    "bwgemm_probe_tensor_rate", "bwgemm_noalloc_scratch", "bwgemm_bench_load_path",
 ]
+
+# layouts of bwgemm_bench_load_path
+LOAD_PATH_LAYOUTS = {0: "128B swizzle", 1: "no swizzle, plain rows (same copies)",
+                     2: "no swizzle, interleaved core matrices (8 copies per tile)"}
 
 # timeline slots of bwgemm_plan_read_trace
 TRACE_ENTRY, TRACE_READY, TRACE_FIRST_LOAD, TRACE_LAST_LOAD, TRACE_EPI_DONE, TRACE_EXIT = range(6)
@@ -176,6 +180,10 @@ def load_library(build_if_missing: bool = False):
         lib.bwgemm_probe_tensor_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                                  ctypes.POINTER(i32)]
         lib.bwgemm_probe_tensor_rate.restype = st
+        lib.bwgemm_bench_load_path.argtypes = [ctypes.c_int, i32, i32, i32, i32, i32,
+                                               ctypes.POINTER(ctypes.c_double),
+                                               ctypes.POINTER(ctypes.c_double)]
+        lib.bwgemm_bench_load_path.restype = st
         _lib = lib
         return lib
 
@@ -233,6 +241,19 @@ def probe_tensor_rate(device: int = 0):
     if rc != 0:
         raise BwgemmError(rc, "bwgemm_probe_tensor_rate")
     return rate.value, sms.value
+
+
+def bench_load_path(layout: int, source: int = 0, ctas: int = 0, stages: int = 6, kblocks: int = 4096,
+                    device: int = 0):
+    """(GB/s landed by all CTAs, milliseconds) of bwgemm_bench_load_path."""
+    lib = load_library()
+    gbs = ctypes.c_double(0.0)
+    ms = ctypes.c_double(0.0)
+    rc = lib.bwgemm_bench_load_path(int(device), int(layout), int(source), int(ctas), int(stages),
+                                    int(kblocks), ctypes.byref(gbs), ctypes.byref(ms))
+    if rc != 0:
+        raise BwgemmError(rc, "bwgemm_bench_load_path")
+    return gbs.value, ms.value
 
 
 def check_args(A_ptr, B_ptr, C_ptr, M, N, K, lda, ldb, ldc, dtype=BF16) -> int:

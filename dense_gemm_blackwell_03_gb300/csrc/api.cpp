@@ -317,10 +317,7 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, c
     if (plan->d_trace) {
         if (sel.cfg.grid > plan->trace_ctas)
             return BWGEMM_ERR_UNSUPPORTED;
-        if (cudaMemsetAsync(plan->d_trace, 0, size_t(sel.cfg.grid) * kTraceSlots * sizeof(uint64_t),
-                            stream) != cudaSuccess)
-            return BWGEMM_ERR_CUDA;
-        p.trace = plan->d_trace;
+        p.trace = plan->d_trace;  // each CTA clears its own row at entry
     }
 
     // C for stores of two 32-column chunks: a 3-D view of whole chunks with

@@ -444,7 +444,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
 // a pair follower's loads, counted on the leader's barriers; multicast loads
 // from the other pair; an exchange copy in flight to or from the partner --
 // land before the cluster's shared memory is released.
-__device__ __noinline__ void settle(uint64_t ns)
+static __device__ __noinline__ void settle(uint64_t ns)
 {
     WaitClock clock;
 #pragma unroll 1
@@ -734,6 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
 
     if (threadIdx.x == 0) {
+        if (p.trace) {
+            // this CTA's row of the timeline starts empty (cleared here rather than
+            // by a memset on the stream, which would serialise back-to-back launches)
+            uint64_t* row = p.trace + size_t(blockIdx.x) * kTraceSlots;
+#pragma unroll 1
+            for (int i = 0; i < kTraceSlots; ++i)
+                row[i] = 0ull;
+        }
         trace_mark(p, kTraceEntry);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);   // producer's arrive.expect_tx (+ bytes)
@@ -820,6 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
+            const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
+            const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
             if (first_unit) {
                 // the first unit is known; now wait for the previous kernel
                 ptx::grid_dependency_wait();
@@ -848,8 +858,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            const int a_row = w.m_blk * Cfg::kTileM + int(prank) * kRowsPerCta;
-            const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
             // L2 prefetch of the streamed operand (the one read from DRAM, not
             // shared by the tiles running at the same time) `prefetch` K
             // blocks ahead of the loads: the DRAM reads in flight are then not

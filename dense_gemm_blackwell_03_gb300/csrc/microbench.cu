@@ -1,0 +1,265 @@
+// microbench.cu -- the load path in isolation: TMA copies of GEMM operand
+// tiles into a shared-memory ring, with no MMA.
+//
+// "Writing a Blackwell GEMM by hand" (step 4, the 128B swizzle) isolates the
+// load path with a benchmark that moves the same bytes with the same copies
+// and changes only the shared-memory layout, and finds the swizzled layout
+// several times faster.  This kernel does the same on GB300.  One CTA per SM
+// runs the GEMM's producer/consumer ring: per K block the producer waits for
+// a free stage, arms its full barrier with the stage's bytes and copies a
+// 128-row x 64-element tile of A and one of B into it; the consumer warp
+// waits for the stage to land and frees it at once (no MMA, no shared-memory
+// reads).  Sources: a 16 MiB bf16 matrix that stays in L2 (the L2 ->
+// shared-memory path, the page's measurement), or a 2 GiB one of which
+// every CTA streams rows of its own, each byte once (the HBM -> shared-memory
+// path that the memory-bound decode shapes run on).
+//
+// Layouts (the layout argument):
+//   0  128B swizzle: one copy of box {64, 128} per operand and K block, 16-byte
+//      chunks of each 128-byte row permuted by the row index (the GEMM's own).
+//   1  no swizzle, plain rows: the same copies (box {64, 128}), rows of 128
+//      bytes one after the other.  Only the layout differs from 0.
+//   2  no swizzle, the tensor cores' interleaved K-major layout: 8-row x
+//      16-byte core matrices, each 128-row column of them contiguous; built
+//      by eight copies of box {8, 128} per operand and K block.
+//
+// Every wait is bounded; a run whose waits run out reports BWGEMM_ERR_TIMEOUT
+// after draining the copies it armed.
+#include "gemm_kernel.cuh"
+#include "internal.h"
+
+#include <mutex>
+
+namespace bwgemm {
+namespace {
+
+constexpr int kLpThreads = 64;                              // producer warp, consumer warp
+constexpr int kLpTileBytes = kRowsPerCta * kTileK * 2;      // 16 KiB: one operand tile
+constexpr int kLpStageBytes = 2 * kLpTileBytes;             // A and B of one K block
+constexpr int kLpMaxStages = 6;
+// sources: 0 = 8192 x 1024 bf16 (16 MiB, stays in L2), 1 = 65536 x 16384 (2 GiB)
+constexpr int kLpSrcRows[2] = {8192, 65536};
+constexpr int kLpSrcCols[2] = {1024, 16384};
+// ring + barriers + abort flag + slack to align the base to 1 KiB; more than
+// half an SM's shared memory, so that one CTA runs per SM
+constexpr int kLpSmem = kLpMaxStages * kLpStageBytes + 2 * 8 * kLpMaxStages + 16 + 1024;
+
+struct LoadPathParams {
+    int kblocks;     // K blocks each CTA moves
+    int stages;      // ring depth (1 .. kLpMaxStages)
+    int layout;      // 0, 1, 2 as above
+    int row_blocks;  // 128-row blocks of the source
+    int src_kblocks; // 64-wide K blocks of the source
+    uint64_t timeout_ns;
+    uint32_t* status;
+};
+
+__global__ void __launch_bounds__(kLpThreads, 1)
+    load_path_kernel(const __grid_constant__ CUtensorMap map, const LoadPathParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t ring = base;
+    const uint32_t bar_full = base + kLpMaxStages * kLpStageBytes;  // + 8 * stage
+    const uint32_t bar_empty = bar_full + 8 * kLpMaxStages;          // + 8 * stage
+    volatile uint32_t* abort_flag =
+        reinterpret_cast<volatile uint32_t*>(smem + kLpMaxStages * kLpStageBytes + 16 * kLpMaxStages);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x == 32)
+        ptx::prefetch_tensormap(&map);
+    __syncthreads();
+
+    GemmParams wp;  // the bounded waits read only the limit and the status word
+    wp.timeout_ns = p.timeout_ns;
+    wp.status = p.status;
+    uint32_t armed_mask = 0, armed_parity = 0;
+    // two different 128-row blocks of the source per CTA (in the lower and the
+    // upper half of its rows), walked along K
+    const int half = p.row_blocks / 2;
+    const int a_row = int(blockIdx.x % half) * kRowsPerCta;
+    const int b_row = (half + int(blockIdx.x % half)) * kRowsPerCta;
+
+    if (warp == 0) {
+#pragma unroll 1
+        for (int i = 0; i < p.kblocks; ++i) {
+            const int s = i % S;
+            const uint32_t phase = uint32_t(i / S) & 1u;
+            if (!__all_sync(0xffffffffu, wait_phase(bar_empty + 8 * s, phase ^ 1u, wp, abort_flag, 1u)))
+                break;
+            armed_mask |= 1u << s;
+            armed_parity = (armed_parity & ~(1u << s)) | (phase << s);
+            if (ptx::elect_one()) {
+                const uint32_t fb = bar_full + 8 * s;
+                const uint32_t dA = ring + uint32_t(s * kLpStageBytes);
+                const uint32_t dB = dA + kLpTileBytes;
+                const int kx = ((i + int(blockIdx.x)) % p.src_kblocks) * kTileK;
+                ptx::mbar_arrive_expect_tx(fb, kLpStageBytes);
+                if (p.layout != 2) {
+                    ptx::tma_load_2d(dA, &map, fb, kx, a_row);
+                    ptx::tma_load_2d(dB, &map, fb, kx, b_row);
+                } else {
+                    // one 16-byte K chunk of all 128 rows per copy: a contiguous
+                    // column of sixteen 8 x 16-byte core matrices
+#pragma unroll
+                    for (int j = 0; j < kTileK / 8; ++j) {
+                        ptx::tma_load_2d(dA + uint32_t(j * kRowsPerCta * 16), &map, fb, kx + 8 * j, a_row);
+                        ptx::tma_load_2d(dB + uint32_t(j * kRowsPerCta * 16), &map, fb, kx + 8 * j, b_row);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+#pragma unroll 1
+        for (int i = 0; i < p.kblocks; ++i) {
+            const int s = i % S;
+            const uint32_t phase = uint32_t(i / S) & 1u;
+            if (!__all_sync(0xffffffffu, wait_phase(bar_full + 8 * s, phase, wp, abort_flag, 2u)))
+                break;
+            if (lane == 0)
+                ptx::mbar_arrive(bar_empty + 8 * s);
+            __syncwarp();
+        }
+    }
+    // after an abort, the copies this CTA armed land before its shared memory
+    // is released (bounded), as in the GEMM kernel's teardown
+    __syncthreads();
+    if (*abort_flag && warp == 0) {
+#pragma unroll 1
+        for (int s = 0; s < S; ++s)
+            if ((armed_mask >> s) & 1u)
+                drain_wait(bar_full + 8 * s, (armed_parity >> s) & 1u, kDrainNs);
+        if (lane == 0)
+            settle(kSettleNs);
+    }
+    __syncthreads();
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn lp_encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+}  // namespace
+}  // namespace bwgemm
+
+using namespace bwgemm;
+
+extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, int32_t source, int32_t ctas,
+                                                  int32_t stages, int32_t kblocks, double* gbytes_per_s,
+                                                  double* ms)
+{
+    if (!gbytes_per_s || !ms || layout < 0 || layout > 2 || source < 0 || source > 1 || ctas < 0 ||
+        stages < 1 || stages > kLpMaxStages || kblocks < 1 || kblocks > (1 << 20))
+        return BWGEMM_ERR_INVALID_ARG;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return BWGEMM_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    const int rows = kLpSrcRows[source], cols = kLpSrcCols[source];
+    const size_t src_bytes = size_t(rows) * size_t(cols) * 2;
+    const int grid = ctas > 0 ? ctas : sms;
+    bwgemm_status_t st = BWGEMM_OK;
+    void* src = nullptr;
+    uint32_t* d_status = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    EncodeTiledFn enc = lp_encode_fn();
+    CUtensorMap map;
+    if (major != 10 || minor != 3 || sms <= 0) {
+        st = BWGEMM_ERR_UNSUPPORTED;
+    } else if (grid > sms) {
+        st = BWGEMM_ERR_INVALID_ARG;  // one CTA per SM at most
+    } else if (!enc) {
+        st = BWGEMM_ERR_NO_DEVICE;
+    } else if (cudaMalloc(&src, src_bytes) != cudaSuccess || cudaMalloc(&d_status, sizeof(uint32_t)) != cudaSuccess ||
+               cudaMemset(src, 0, src_bytes) != cudaSuccess ||
+               cudaMemset(d_status, 0, sizeof(uint32_t)) != cudaSuccess ||
+               cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
+               cudaFuncSetAttribute(load_path_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLpSmem) !=
+                   cudaSuccess) {
+        cudaGetLastError();
+        st = BWGEMM_ERR_CUDA;
+    } else {
+        const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+        const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+        const cuuint32_t box[2] = {uint32_t(layout == 2 ? 8 : kTileK), uint32_t(kRowsPerCta)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                layout == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            st = BWGEMM_ERR_CUDA;
+    }
+    if (st == BWGEMM_OK) {
+        LoadPathParams p;
+        p.kblocks = kblocks;
+        p.stages = stages;
+        p.layout = layout;
+        p.row_blocks = rows / kRowsPerCta;
+        p.src_kblocks = cols / kTileK;
+        p.timeout_ns = 2000000000ull;
+        p.status = d_status;
+        // a warm-up launch (tensor map; the L2 source filled), then the timed one
+        load_path_kernel<<<grid, kLpThreads, kLpSmem>>>(map, p);
+        cudaEventRecord(e0);
+        load_path_kernel<<<grid, kLpThreads, kLpSmem>>>(map, p);
+        cudaEventRecord(e1);
+        uint32_t h_status = 0;
+        float t = 0.f;
+        if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&t, e0, e1) != cudaSuccess ||
+            cudaMemcpy(&h_status, d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+            st = BWGEMM_ERR_CUDA;
+        else if (h_status != 0)
+            st = BWGEMM_ERR_TIMEOUT;
+        else if (t <= 0.f)
+            st = BWGEMM_ERR_CUDA;
+        else {
+            *ms = double(t);
+            *gbytes_per_s = double(grid) * double(kblocks) * double(kLpStageBytes) / (double(t) * 1e-3) / 1e9;
+        }
+    }
+    if (e0)
+        cudaEventDestroy(e0);
+    if (e1)
+        cudaEventDestroy(e1);
+    if (src)
+        cudaFree(src);
+    if (d_status)
+        cudaFree(d_status);
+    cudaSetDevice(prev);
+    return st;
+}

@@ -304,6 +304,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     // K blocks (one or two K blocks per prefetch) it was slower every time.
     sel.cfg.prefetch_kblocks = opts.prefetch > 0 ? opts.prefetch : 0;
     sel.cfg.prefetch_b = (Nk >= Mk) ? 1 : 0;
+
     *out = sel;
     return BWGEMM_OK;
 }

@@ -38,6 +38,42 @@ def units(trace: np.ndarray):
     return out
 
 
+def epilogue_share(trace: np.ndarray) -> dict:
+    """How much of a launch the epilogue takes ("Writing a Blackwell GEMM by
+    hand", step 5: measure a stage's share of the kernel before optimising
+    it), from the stamps of an unmodified launch:
+
+    - busy: the epilogue warps' time with an accumulator in hand (from seeing
+      it ready to the unit's last store issued), summed over a CTA's units,
+      as a share of the launch's span; the TMEM double buffer overlaps most of
+      it with the next unit's MMAs;
+    - exposed: per CTA, the time from its last MMA commit to the end of its
+      last epilogue, which nothing overlaps; as microseconds and as a share
+      of the span.
+    """
+    tr = np.asarray(trace, dtype=np.int64)
+    tr = tr[tr[:, TRACE_ENTRY] > 0]
+    if tr.shape[0] == 0:
+        return {"ctas": 0}
+    span = float(tr[:, TRACE_EXIT].max() - tr[:, TRACE_ENTRY].min())
+    busy, exposed = [], []
+    for ulist in units(tr):
+        done = [u for u in ulist if u[2] > 0 and u[3] > 0]
+        if not done:
+            continue
+        busy.append(sum(u[3] - u[2] for u in done))
+        last_commit = max((u[1] for u in ulist if u[1] > 0), default=0)
+        if last_commit:
+            exposed.append(max(0, max(u[3] for u in done) - last_commit))
+    if not busy or span <= 0:
+        return {"ctas": int(tr.shape[0])}
+    return {"ctas": int(tr.shape[0]), "span_us": round(span / 1e3, 3),
+            "busy_us_per_cta": round(float(np.mean(busy)) / 1e3, 3),
+            "busy_share": round(float(np.mean(busy)) / span, 4),
+            "exposed_us": round(float(np.mean(exposed)) / 1e3, 3) if exposed else None,
+            "exposed_share": round(float(np.mean(exposed)) / span, 4) if exposed else None}
+
+
 def summarize(trace: np.ndarray) -> dict:
     """Phase durations in microseconds over all CTAs of one launch."""
     tr = np.asarray(trace, dtype=np.int64)
@@ -119,7 +155,7 @@ def main(argv=None) -> int:
         cfg = plan.last_config()
     spans = [(u[1] - u[0]) / 1e3 for row in units(trace) for u in row if u[0] and u[1]]
     out = {"shape": args.shape, "config": cfg, "summary": summarize(trace),
-           "mma_span_us_per_unit": _stat(spans)}
+           "mma_span_us_per_unit": _stat(spans), "epilogue": epilogue_share(trace)}
     print(json.dumps(out))
     return 0
 

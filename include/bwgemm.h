@@ -250,7 +250,10 @@ bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out
  * per work unit (at most 14 units): MMA start, MMA end, epilogue start,
  * epilogue end.  *ctas and *slots receive the dimensions; `capacity` is the
  * size of `out` in elements.  BWGEMM_ERR_INVALID_ARG if tracing is off or
- * `out` is too small.
+ * `out` is too small.  Each CTA clears its own row as it starts, so tracing
+ * adds nothing to the stream between launches; two launches of one traced
+ * plan that overlap (programmatic dependent launch) write the same rows, so
+ * for a timeline of back-to-back launches alternate two traced plans.
  */
 bwgemm_status_t bwgemm_plan_read_trace(bwgemm_plan_t plan, uint64_t* out, int64_t capacity,
                                        int32_t* ctas, int32_t* slots);
@@ -272,6 +275,33 @@ uint64_t bwgemm_plan_launch_count(bwgemm_plan_t plan);
  * (the bounded wait for the MMAs ran out).
  */
 bwgemm_status_t bwgemm_probe_tensor_rate(int device, double* flop_per_clock_per_sm, int32_t* sm_count);
+
+/*
+ * Load-path microbenchmark ("Writing a Blackwell GEMM by hand", step 4: a
+ * benchmark that isolates the load path, with no MMA, moving the same bytes
+ * with the same copies and changing only the shared-memory layout).  `ctas`
+ * CTAs (0 = one per SM of `device`; at most one per SM) run the GEMM's ring
+ * of `stages` (1..6) stages of 32 KiB: per K block the producer copies a
+ * 128-row x 64-element bf16 tile of A and one of B by TMA and a consumer
+ * warp frees the stage as soon as it lands, for `kblocks` (1..2^20) K blocks
+ * per CTA.  `source`: 0 = a 16 MiB matrix that stays in L2 (the L2 ->
+ * shared-memory path), 1 = a 2 GiB matrix of which every CTA streams rows
+ * of its own (the HBM -> shared-memory path; 256 K blocks per row block
+ * before a CTA wraps).  `layout`: 0 = 128B swizzle (the GEMM's layout, one
+ * copy of box {64, 128} per tile), 1 = no swizzle with the same copies
+ * (plain 128-byte rows), 2 = no swizzle in the tensor cores' interleaved
+ * K-major layout (8 x 16-byte core matrices, eight copies of box {8, 128}
+ * per tile).  Writes the bytes landed by all CTAs per second (GB/s, one
+ * timed launch after a warm-up launch, CUDA events) to *gbytes_per_s and the
+ * launch's time to *ms.  Allocates and frees its source matrix; synchronises
+ * the device.  Errors: BWGEMM_ERR_INVALID_ARG (NULL output or an argument
+ * out of range, more CTAs than SMs), BWGEMM_ERR_NO_DEVICE,
+ * BWGEMM_ERR_UNSUPPORTED (not sm_103), BWGEMM_ERR_CUDA, BWGEMM_ERR_TIMEOUT (a
+ * bounded wait ran out).
+ */
+bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, int32_t source, int32_t ctas,
+                                       int32_t stages, int32_t kblocks, double* gbytes_per_s,
+                                       double* ms);
 
 /*
  * Shape-keyed tuning ("Matrix Multiplication on NVIDIA's Blackwell", the

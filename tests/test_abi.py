@@ -436,3 +436,14 @@ def test_noalloc_scratch_stays_inside_the_array(lib):
     assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 1, ctypes.byref(p), ctypes.byref(c)) == INVALID
     assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 17, ctypes.byref(p), ctypes.byref(c)) == INVALID
     assert lib.bwgemm_noalloc_scratch(148, 74, 256, 512, 1600, 2, None, ctypes.byref(c)) == INVALID
+
+
+def test_bench_load_path_rejects_bad_arguments(lib):
+    # argument checks come before any device access (no GPU needed)
+    gbs, ms = ctypes.c_double(), ctypes.c_double()
+    for layout, source, ctas, stages, kblocks in ((3, 0, 0, 6, 64), (-1, 0, 0, 6, 64), (0, 2, 0, 6, 64),
+                                                  (0, -1, 0, 6, 64), (0, 0, -1, 6, 64), (0, 0, 0, 0, 64),
+                                                  (0, 0, 0, 7, 64), (0, 0, 0, 6, 0)):
+        assert lib.bwgemm_bench_load_path(0, layout, source, ctas, stages, kblocks, ctypes.byref(gbs),
+                                          ctypes.byref(ms)) == INVALID
+    assert lib.bwgemm_bench_load_path(0, 0, 0, 0, 6, 64, None, ctypes.byref(ms)) == INVALID

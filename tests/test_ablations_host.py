@@ -48,3 +48,39 @@ def test_markdown_table_from_rows():
                         "1068.0 | 0.654 | 1 |")
     assert lines[3].endswith("| 40.34 | 851.9 | 0.522 | 0.798 |")
     assert "default (swapped, 1 CTA, 64, split-K 2 in clusters)" in lines[4]
+
+
+def test_load_path_and_epilogue_tables():
+    lp = [{"kind": "load_path", "layout": 0, "row": "128B swizzle", "copies_per_stage": 2, "gbs": 20000.0,
+           "vs_swizzle": 1.0},
+          {"kind": "load_path", "layout": 1, "row": "no swizzle, plain rows (same copies)",
+           "copies_per_stage": 2, "gbs": 5000.0, "vs_swizzle": 0.25}]
+    lines = ablations.load_path_table(lp).splitlines()
+    assert len(lines) == 4
+    assert lines[2] == "| 128B swizzle | 2 | 20.00 | 1.000 | 18.5 |"
+    assert lines[3].endswith("| 5.00 | 0.250 | 3.85 |")
+    ep = [{"kind": "epilogue_share", "shape": "square4096", "units_per_cta": 2.5,
+           "epilogue": {"span_us": 84.0, "busy_us_per_cta": 9.0, "busy_share": 0.1071,
+                        "exposed_us": 3.0, "exposed_share": 0.0357}}]
+    lines = ablations.epilogue_table(ep).splitlines()
+    assert lines[2] == "| 4096^3 | 84.00 | 2.50 | 9.00 | 0.107 | 3.00 | 0.036 |"
+
+
+def test_epilogue_share_from_stamps():
+    import numpy as np
+
+    from dense_gemm_blackwell_03_gb300 import timeline
+    from dense_gemm_blackwell_03_gb300.binding import (TRACE_ENTRY, TRACE_EXIT, TRACE_UNIT0,
+                                                       TRACE_UNITS)
+    tr = np.zeros((2, TRACE_UNIT0 + 4 * TRACE_UNITS), dtype=np.uint64)
+    # CTA 0: two units; MMAs 1000-5000 and 5000-9000 ns, epilogues 5100-6100 and 9100-10100
+    tr[0, TRACE_ENTRY], tr[0, TRACE_EXIT] = 1000, 10500
+    tr[0, TRACE_UNIT0:TRACE_UNIT0 + 8] = [1000, 5000, 5100, 6100, 5000, 9000, 9100, 10100]
+    # CTA 1: one unit, epilogue 500 ns after its last commit
+    tr[1, TRACE_ENTRY], tr[1, TRACE_EXIT] = 1000, 11000
+    tr[1, TRACE_UNIT0:TRACE_UNIT0 + 4] = [1200, 9500, 9600, 10000]
+    e = timeline.epilogue_share(tr)
+    assert e["ctas"] == 2 and e["span_us"] == 10.0
+    assert e["busy_us_per_cta"] == round((2000 + 400) / 2 / 1e3, 3)
+    assert e["exposed_us"] == round((1100 + 500) / 2 / 1e3, 3)
+    assert e["exposed_share"] == round(800 / 10000, 4)

@@ -691,3 +691,22 @@ def test_probe_tensor_rate():
         measured = json.load(open(path)).get("bf16_tflops")
         if measured:
             assert sms * rate * max_mhz * 1e6 / 1e12 >= 0.95 * float(measured)
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+@pytest.mark.parametrize("source,ctas", [(0, 0), (1, 0), (1, 64)])
+def test_load_path_microbench(layout, source, ctas):
+    # the load path alone (no MMA) in each shared-memory layout, from L2 and
+    # from HBM: every wait ends, and the landed bytes per second are plausible
+    binding.load_library(build_if_missing=True)
+    gbs, ms = binding.bench_load_path(layout, source=source, ctas=ctas, stages=6, kblocks=256)
+    assert ms > 0 and 100.0 < gbs < 200000.0
+
+
+def test_epilogue_share_of_a_traced_launch():
+    from dense_gemm_blackwell_03_gb300 import ablations
+    (row,) = ablations.run_epilogue_share(["square512"], warmup=2)
+    e = row["epilogue"]
+    assert e["ctas"] > 0 and 0.0 < e["busy_share"] <= 1.0
+    assert e["exposed_us"] is not None and 0.0 <= e["exposed_share"] <= 1.0
+

@@ -42,10 +42,13 @@ EXPORTED = [
 
 # layouts of bwgemm_bench_load_path
 LOAD_PATH_LAYOUTS = {0: "128B swizzle", 1: "no swizzle, plain rows (same copies)",
-                     2: "no swizzle, interleaved core matrices (8 copies per tile)"}
+                     2: "no swizzle, interleaved core matrices (8 copies per tile)",
+                     3: "128B swizzle, one 256-row copy per K block",
+                     4: "128B swizzle, A multicast in halves across two CTAs"}
 
 # timeline slots of bwgemm_plan_read_trace
-TRACE_ENTRY, TRACE_READY, TRACE_FIRST_LOAD, TRACE_LAST_LOAD, TRACE_EPI_DONE, TRACE_EXIT = range(6)
+(TRACE_ENTRY, TRACE_READY, TRACE_FIRST_LOAD, TRACE_LAST_LOAD, TRACE_EPI_DONE, TRACE_EXIT, TRACE_SETUP,
+ TRACE_UNIT_KNOWN) = range(8)
 TRACE_UNIT0 = 8
 TRACE_UNITS = 14
 

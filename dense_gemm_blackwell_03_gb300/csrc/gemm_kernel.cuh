@@ -168,10 +168,17 @@ __device__ __forceinline__ int slice_begin(int i, int kb, int S)
     return int((long long)i * kb / S);
 }
 
-// First stream-K iteration of `worker` (of `workers`).
+// First stream-K iteration of `worker` (of `workers`): in 32-bit arithmetic
+// when the product fits (a 64-bit division is a long subroutine on the
+// critical path of every CTA's start), none at all without stream-K.
 __device__ __forceinline__ long long sk_begin(const GemmParams& p, int worker, int workers)
 {
-    return (long long)worker * p.sk_iters / workers;
+    if (p.sk_iters == 0)
+        return 0;
+    const long long prod = (long long)worker * p.sk_iters;
+    if (prod < (1ll << 32))
+        return (long long)(unsigned(prod) / unsigned(workers));
+    return prod / workers;
 }
 
 // The worker whose stream-K range holds iteration `it`.
@@ -733,7 +740,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
 
-    if (threadIdx.x == 0) {
+    // Set-up runs in three warps at once: warp 3 (an epilogue warp, idle until
+    // the first accumulator is ready) initialises the barriers, warp 1
+    // allocates TMEM, warp 0 prefetches the tensor maps; meanwhile every role
+    // works out its first work unit (below), which used to follow the set-up
+    // and delayed the first loads of the CTAs that start last.
+    constexpr int kInitThread = 3 * 32;
+    if (threadIdx.x == kInitThread) {
         if (p.trace) {
             // this CTA's row of the timeline starts empty (cleared here rather than
             // by a memset on the stream, which would serialise back-to-back launches)
@@ -780,6 +793,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
         ptx::tmem_relinquish<CG>();
     }
+    // Every role walks the same unit sequence; the first unit is pure
+    // arithmetic on the launch parameters (or, with cluster launch control, the
+    // cluster's own index).  The producer and the MMA warp work theirs out now,
+    // each into its own scheduler (dead in the other roles' code, so it costs
+    // the epilogue no registers); the epilogue has until the first
+    // accumulator is ready and works its out after the set-up.
+    const uint32_t clc_empty_leader = (CS > 1) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
+    Sched iter_p, iter_m;
+    WorkUnit w0_p{}, w0_m{};
+    bool have0_p = false, have0_m = false;
+    if (warp == 0) {
+        iter_p.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
+        have0_p = iter_p.next<CG, true>(p, w0_p, false, abort_flag, 0u);
+    } else if (warp == 1 && prank == 0) {
+        iter_m.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
+        have0_m = iter_m.next<CG, true>(p, w0_m, false, abort_flag, 0u);
+    }
     ptx::tc_fence_before_sync();
     if constexpr (CS > 1)
         ptx::cluster_sync();
@@ -787,6 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == kInitThread)
+        trace_mark(p, kTraceSetup);
 
     // Everything above may overlap the previous kernel on the stream
     // (programmatic dependent launch), and so may each role's set-up below:
@@ -794,7 +826,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before its first access to global memory.  The next kernel may be
     // scheduled from here on.
     ptx::launch_dependents();
-    const uint32_t clc_empty_leader = (CS > 1) ? ptx::map_to_cta(bar_clc_empty, 0) : bar_clc_empty;
     // producer (warp 0) of a CTA whose full barriers count its loads (one CTA,
     // or a pair leader): stages armed with a load, and the parity of the phase
     // each last armed fill completes -- what the abort drain waits for
@@ -813,12 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         bool first_unit = true;
         int requested = 0;
-        Sched iter;
-        iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
-        WorkUnit w;
+        Sched iter = iter_p;
+        WorkUnit w = w0_p;
         // both CTAs' bytes of a pair are counted on the pair leader's barrier
         const uint32_t leader_full = (CG == 2) ? ptx::map_to_cta(bar_full, leader) : bar_full;
-        while (ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusProducerTimeout)) {
+        for (bool have = have0_p; ok && have;
+             have = ok && iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusProducerTimeout)) {
             if constexpr (RS) {
                 // a ring-staged kernel runs one unit per CTA: a second one would
                 // refill the ring its epilogue stages in -- a planning error
@@ -832,6 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b_row = w.n_blk * BN + int(prank) * Cfg::kBRows;
             if (first_unit) {
                 // the first unit is known; now wait for the previous kernel
+                if (lane == 0)
+                    trace_mark(p, kTraceUnitKnown);
                 ptx::grid_dependency_wait();
                 if (lane == 0)
                     trace_mark(p, kTraceReady);
@@ -992,9 +1025,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int t = 0;
             bool ok = true;
-            Sched iter;
-            iter.init(p, worker, workers, CS, MC, int(pair), clc_resp, bar_clc_full, clc_empty_leader);
-            WorkUnit w;
+            Sched iter = iter_m;
+            WorkUnit w = w0_m;
             // Without launch control the unit sequence is pure arithmetic (a few
             // dependent integer divisions, ~0.5 us): the next unit is worked out
             // right after the current unit's first K block is issued, while the
@@ -1002,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // pipe idle.  With launch control it waits for a response and stays
             // between units.
             const bool ahead = !p.clc;
-            bool have = iter.next<CG, true>(p, w, lane == 0, abort_flag, kStatusMmaTimeout);
+            bool have = have0_m;
             WorkUnit w_next;
             bool have_next = false;
             while (ok && have) {

@@ -92,6 +92,8 @@ enum : int {
     kTraceLastLoad = 3,       // producer issued its last TMA load
     kTraceEpiDone = 4,        // epilogue warp 2 finished (stores complete)
     kTraceExit = 5,           // teardown done
+    kTraceSetup = 6,          // barriers, TMEM and the cluster barrier of the prologue done
+    kTraceUnitKnown = 7,      // producer worked out its first unit (before the dependency wait)
     kTraceUnit0 = 8,          // then per unit u < kTraceUnits: MMA start, MMA end,
     kTraceUnits = 14,         //   epilogue start, epilogue end (4 slots each)
     kTraceSlots = kTraceUnit0 + 4 * kTraceUnits,

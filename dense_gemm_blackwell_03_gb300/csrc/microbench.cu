@@ -22,6 +22,12 @@
 //   2  no swizzle, the tensor cores' interleaved K-major layout: 8-row x
 //      16-byte core matrices, each 128-row column of them contiguous; built
 //      by eight copies of box {8, 128} per operand and K block.
+//   3  128B swizzle, one copy of box {64, 256} per K block (A's and B's rows
+//      adjacent in the source): the same bytes in half the copies.
+//   4  128B swizzle, clusters of two CTAs sharing A: each CTA copies half of
+//      the A tile (box {64, 64}) with cluster multicast into both CTAs and
+//      its own B tile (box {64, 128}); every CTA still receives 32 KiB per
+//      K block but issues 24 KiB (the GEMM's multicast of a shared operand).
 //
 // Every wait is bounded; a run whose waits run out reports BWGEMM_ERR_TIMEOUT
 // after draining the copies it armed.
@@ -55,7 +61,8 @@ struct LoadPathParams {
 };
 
 __global__ void __launch_bounds__(kLpThreads, 1)
-    load_path_kernel(const __grid_constant__ CUtensorMap map, const LoadPathParams p)
+    load_path_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap map2,
+                     const LoadPathParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -69,18 +76,27 @@ __global__ void __launch_bounds__(kLpThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
+    const bool mc = p.layout == 4;  // launched in clusters of two CTAs
+    const uint32_t rank = mc ? ptx::cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, 1);
+            // with multicast a stage is free once the consumers of both CTAs freed it
+            ptx::mbar_init(bar_empty + 8 * s, mc ? 2 : 1);
         }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
-    if (threadIdx.x == 32)
+    if (threadIdx.x == 32) {
         ptx::prefetch_tensormap(&map);
-    __syncthreads();
+        if (p.layout >= 3)
+            ptx::prefetch_tensormap(&map2);
+    }
+    if (mc)
+        ptx::cluster_sync();  // the partner's barriers are initialised before any multicast
+    else
+        __syncthreads();
 
     GemmParams wp;  // the bounded waits read only the limit and the status word
     wp.timeout_ns = p.timeout_ns;
@@ -107,7 +123,15 @@ __global__ void __launch_bounds__(kLpThreads, 1)
                 const uint32_t dB = dA + kLpTileBytes;
                 const int kx = ((i + int(blockIdx.x)) % p.src_kblocks) * kTileK;
                 ptx::mbar_arrive_expect_tx(fb, kLpStageBytes);
-                if (p.layout != 2) {
+                if (p.layout == 3) {
+                    // A's and B's 128-row blocks as one 256-row box
+                    ptx::tma_load_2d(dA, &map2, fb, kx, a_row);
+                } else if (p.layout == 4) {
+                    // this CTA's half of the shared A tile into both CTAs, its own B
+                    ptx::tma_load_2d_multicast(dA + rank * uint32_t(kLpTileBytes / 2), &map2, fb, kx,
+                                               a_row + int(rank) * (kRowsPerCta / 2), uint16_t(0x3u));
+                    ptx::tma_load_2d(dB, &map, fb, kx, b_row);
+                } else if (p.layout != 2) {
                     ptx::tma_load_2d(dA, &map, fb, kx, a_row);
                     ptx::tma_load_2d(dB, &map, fb, kx, b_row);
                 } else {
@@ -129,8 +153,11 @@ __global__ void __launch_bounds__(kLpThreads, 1)
             const uint32_t phase = uint32_t(i / S) & 1u;
             if (!__all_sync(0xffffffffu, wait_phase(bar_full + 8 * s, phase, wp, abort_flag, 2u)))
                 break;
-            if (lane == 0)
+            if (lane == 0) {
                 ptx::mbar_arrive(bar_empty + 8 * s);
+                if (mc)  // the partner multicasts into this stage too
+                    ptx::mbar_arrive_cluster(ptx::map_to_cta(bar_empty + 8 * s, rank ^ 1u));
+            }
             __syncwarp();
         }
     }
@@ -145,7 +172,12 @@ __global__ void __launch_bounds__(kLpThreads, 1)
         if (lane == 0)
             settle(kSettleNs);
     }
-    __syncthreads();
+    // with multicast, neither CTA leaves while the other may still copy into it
+    // or arrive on its barriers
+    if (mc)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -177,7 +209,7 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
                                                   int32_t stages, int32_t kblocks, double* gbytes_per_s,
                                                   double* ms)
 {
-    if (!gbytes_per_s || !ms || layout < 0 || layout > 2 || source < 0 || source > 1 || ctas < 0 ||
+    if (!gbytes_per_s || !ms || layout < 0 || layout > 4 || source < 0 || source > 1 || ctas < 0 ||
         stages < 1 || stages > kLpMaxStages || kblocks < 1 || kblocks > (1 << 20))
         return BWGEMM_ERR_INVALID_ARG;
     int prev = 0;
@@ -191,16 +223,17 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     const int rows = kLpSrcRows[source], cols = kLpSrcCols[source];
     const size_t src_bytes = size_t(rows) * size_t(cols) * 2;
-    const int grid = ctas > 0 ? ctas : sms;
+    // clusters of two CTAs for layout 4: an even number of CTAs
+    const int grid = (ctas > 0 ? ctas : sms) & (layout == 4 ? ~1 : ~0);
     bwgemm_status_t st = BWGEMM_OK;
     void* src = nullptr;
     uint32_t* d_status = nullptr;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     EncodeTiledFn enc = lp_encode_fn();
-    CUtensorMap map;
+    CUtensorMap map, map2;
     if (major != 10 || minor != 3 || sms <= 0) {
         st = BWGEMM_ERR_UNSUPPORTED;
-    } else if (grid > sms) {
+    } else if (grid > sms || grid < 1) {
         st = BWGEMM_ERR_INVALID_ARG;  // one CTA per SM at most
     } else if (!enc) {
         st = BWGEMM_ERR_NO_DEVICE;
@@ -217,10 +250,15 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
         const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
         const cuuint32_t box[2] = {uint32_t(layout == 2 ? 8 : kTileK), uint32_t(kRowsPerCta)};
         const cuuint32_t estr[2] = {1, 1};
+        // second map: the 256-row box of layout 3, the 64-row half of layout 4
+        const cuuint32_t box2[2] = {uint32_t(kTileK), uint32_t(layout == 3 ? 2 * kRowsPerCta : kRowsPerCta / 2)};
+        const bool swz = layout == 0 || layout >= 3;
         if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE,
-                layout == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box2, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             st = BWGEMM_ERR_CUDA;
     }
     if (st == BWGEMM_OK) {
@@ -232,10 +270,21 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
         p.src_kblocks = cols / kTileK;
         p.timeout_ns = 2000000000ull;
         p.status = d_status;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(grid), 1, 1);
+        cfg.blockDim = dim3(kLpThreads, 1, 1);
+        cfg.dynamicSmemBytes = kLpSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = layout == 4 ? 2 : 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         // a warm-up launch (tensor map; the L2 source filled), then the timed one
-        load_path_kernel<<<grid, kLpThreads, kLpSmem>>>(map, p);
+        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, p);
         cudaEventRecord(e0);
-        load_path_kernel<<<grid, kLpThreads, kLpSmem>>>(map, p);
+        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, p);
         cudaEventRecord(e1);
         uint32_t h_status = 0;
         float t = 0.f;

@@ -233,6 +233,19 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const C
         : "memory");
 }
 
+// Plain (one-CTA) load with cluster multicast: one read of the box lands at
+// the same shared-memory offset in every CTA of `cta_mask`, each counting the
+// bytes on its barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                      int32_t c0, int32_t c1, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+
 // Prefetch one 2-D box of a tensor into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1)
 {

@@ -246,7 +246,9 @@ bwgemm_status_t bwgemm_plan_last_config(bwgemm_plan_t plan, bwgemm_config_t* out
  * synchronises the device, then copies ctas x slots %globaltimer stamps
  * (nanoseconds; 0 = not reached) into `out`, row per CTA.  Slots: 0 kernel
  * entry, 1 prologue and dependency wait done, 2 first TMA load issued,
- * 3 last TMA load issued, 4 epilogue finished, 5 exit; from slot 8 on, four
+ * 3 last TMA load issued, 4 epilogue finished, 5 exit, 6 barriers, TMEM and
+ * the prologue's cluster barrier done, 7 producer's first unit worked out
+ * (before the dependency wait); from slot 8 on, four
  * per work unit (at most 14 units): MMA start, MMA end, epilogue start,
  * epilogue end.  *ctas and *slots receive the dimensions; `capacity` is the
  * size of `out` in elements.  BWGEMM_ERR_INVALID_ARG if tracing is off or
@@ -291,7 +293,11 @@ bwgemm_status_t bwgemm_probe_tensor_rate(int device, double* flop_per_clock_per_
  * copy of box {64, 128} per tile), 1 = no swizzle with the same copies
  * (plain 128-byte rows), 2 = no swizzle in the tensor cores' interleaved
  * K-major layout (8 x 16-byte core matrices, eight copies of box {8, 128}
- * per tile).  Writes the bytes landed by all CTAs per second (GB/s, one
+ * per tile), 3 = 128B swizzle with one copy of box {64, 256} per K block
+ * (the same bytes in half the copies), 4 = 128B swizzle in clusters of two
+ * CTAs that share A: each copies half of the A tile with cluster multicast
+ * into both and its own B tile (the same bytes landed, three quarters
+ * issued; an even number of CTAs).  Writes the bytes landed by all CTAs per second (GB/s, one
  * timed launch after a warm-up launch, CUDA events) to *gbytes_per_s and the
  * launch's time to *ms.  Allocates and frees its source matrix; synchronises
  * the device.  Errors: BWGEMM_ERR_INVALID_ARG (NULL output or an argument

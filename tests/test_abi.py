@@ -441,7 +441,7 @@ def test_noalloc_scratch_stays_inside_the_array(lib):
 def test_bench_load_path_rejects_bad_arguments(lib):
     # argument checks come before any device access (no GPU needed)
     gbs, ms = ctypes.c_double(), ctypes.c_double()
-    for layout, source, ctas, stages, kblocks in ((3, 0, 0, 6, 64), (-1, 0, 0, 6, 64), (0, 2, 0, 6, 64),
+    for layout, source, ctas, stages, kblocks in ((5, 0, 0, 6, 64), (-1, 0, 0, 6, 64), (0, 2, 0, 6, 64),
                                                   (0, -1, 0, 6, 64), (0, 0, -1, 6, 64), (0, 0, 0, 0, 64),
                                                   (0, 0, 0, 7, 64), (0, 0, 0, 6, 0)):
         assert lib.bwgemm_bench_load_path(0, layout, source, ctas, stages, kblocks, ctypes.byref(gbs),

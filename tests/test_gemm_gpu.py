@@ -693,7 +693,7 @@ def test_probe_tensor_rate():
             assert sms * rate * max_mhz * 1e6 / 1e12 >= 0.95 * float(measured)
 
 
-@pytest.mark.parametrize("layout", [0, 1, 2])
+@pytest.mark.parametrize("layout", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("source,ctas", [(0, 0), (1, 0), (1, 64)])
 def test_load_path_microbench(layout, source, ctas):
     # the load path alone (no MMA) in each shared-memory layout, from L2 and

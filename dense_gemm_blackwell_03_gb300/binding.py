@@ -78,7 +78,8 @@ class PlanOptions(ctypes.Structure):
         ("multicast", ctypes.c_int32),
         ("copy_kblocks", ctypes.c_int32),
         ("cluster_split", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("tuned_table", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 
@@ -106,6 +107,7 @@ class Config(ctypes.Structure):
         ("prefetch_kblocks", ctypes.c_int32),
         ("prefetch_b", ctypes.c_int32),
         ("cluster_split", ctypes.c_int32),
+        ("tuned", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -623,30 +623,46 @@ bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, vo
         return BWGEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // Candidates: the plan's options with one or two choices overridden.  Each
-    // is planned on the host first; ones that fail to plan or plan to a
-    // configuration already seen are skipped.
+    // Candidates: the plan's options with one to three choices overridden
+    // (-1 = keep).  Each is planned on the host first; ones that fail to plan
+    // or plan to a configuration already seen are skipped.
     struct Override {
-        int32_t variant, tile_n, split_k, schedule, copy_kblocks, cluster_split, raster_group, swap_ab;
+        int32_t variant, tile_n, split_k, schedule, copy_kblocks, cluster_split, raster_group, swap_ab,
+            multicast;
     };
+    constexpr int32_t X = -1;
     const Override kCandidates[] = {
-        {-1, -1, -1, -1, -1, -1, -1, -1},  // the plan's own choice
-        {-1, -1, 1, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
-        {-1, -1, -1, BWGEMM_SCHEDULE_STREAM_K, -1, -1, -1, -1},
-        {-1, -1, 2, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
-        {-1, -1, 3, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
-        {-1, -1, 4, BWGEMM_SCHEDULE_TILES, -1, -1, -1, -1},
-        {-1, -1, -1, -1, 1, -1, -1, -1},
-        {-1, -1, -1, -1, 2, -1, -1, -1},
-        {-1, -1, -1, -1, -1, 1, -1, -1},
-        {-1, 128, -1, -1, -1, -1, -1, -1},
-        {BWGEMM_VARIANT_1SM, -1, -1, -1, -1, -1, -1, -1},
-        {BWGEMM_VARIANT_1SM, 128, -1, -1, -1, -1, -1, -1},
-        {-1, -1, -1, -1, -1, -1, 4, -1},
-        {-1, -1, -1, -1, -1, -1, 16, -1},
-        {-1, -1, -1, -1, -1, -1, -1, 1},
-        {-1, -1, -1, -1, -1, -1, -1, 2},
-        {-1, -1, -1, BWGEMM_SCHEDULE_CLC, -1, -1, -1, -1},
+        {X, X, X, X, X, X, X, X, X},  // the plan's own choice
+        // schedule and split
+        {X, X, 1, BWGEMM_SCHEDULE_TILES, X, X, X, X, X},
+        {X, X, X, BWGEMM_SCHEDULE_STREAM_K, X, X, X, X, X},
+        {X, X, 2, BWGEMM_SCHEDULE_TILES, X, X, X, X, X},
+        {X, X, 3, BWGEMM_SCHEDULE_TILES, X, X, X, X, X},
+        {X, X, 4, BWGEMM_SCHEDULE_TILES, X, X, X, X, X},
+        {X, X, X, BWGEMM_SCHEDULE_CLC, X, X, X, X, X},
+        {X, X, X, X, X, 1, X, X, X},  // split-K through L2 instead of in a cluster
+        // copies per K block
+        {X, X, X, X, 1, X, X, X, X},
+        {X, X, X, X, 2, X, X, X, X},
+        // tile shape: one CTA, narrower or wider pair tiles (the planner's own
+        // widths 224 / 320 / 384 and the plain 256 in either direction)
+        {X, 128, X, X, X, X, X, X, X},
+        {BWGEMM_VARIANT_1SM, X, X, X, X, X, X, X, X},
+        {BWGEMM_VARIANT_1SM, 128, X, X, X, X, X, X, X},
+        {BWGEMM_VARIANT_2SM, 224, X, X, X, X, X, 1, X},
+        {BWGEMM_VARIANT_2SM, 224, 2, BWGEMM_SCHEDULE_TILES, X, X, X, 1, X},
+        {BWGEMM_VARIANT_2SM, 256, X, X, X, X, X, 1, X},
+        {BWGEMM_VARIANT_2SM, 320, X, X, X, X, X, 1, X},
+        {BWGEMM_VARIANT_2SM, 384, X, X, X, X, X, 1, X},
+        // A multicast across two CTA pairs
+        {BWGEMM_VARIANT_2SM, 256, X, X, X, X, X, 1, 2},
+        {BWGEMM_VARIANT_2SM, 128, X, X, X, X, X, 1, 2},
+        // raster group and operand order
+        {X, X, X, X, X, X, 2, X, X},
+        {X, X, X, X, X, X, 4, X, X},
+        {X, X, X, X, X, X, 16, X, X},
+        {X, X, X, X, X, X, X, 1, X},
+        {X, X, X, X, X, X, X, 2, X},
     };
     const int pairs = plan->max_active[find_variant(2, 256, false, 1)];
     const int quads = plan->max_active[find_variant(2, 256, false, 2)];
@@ -656,6 +672,7 @@ bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, vo
         bwgemm_plan_options_t opts = plan->opts;
         opts.trace = 0;
         opts.stall_kblock = -1;
+        opts.tuned_table = 1;  // the candidates are the rules' choices and their variations
         if (o.variant >= 0) opts.variant = o.variant;
         if (o.tile_n >= 0) opts.tile_n = o.tile_n;
         if (o.split_k >= 0) opts.split_k = o.split_k;
@@ -664,6 +681,7 @@ bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, vo
         if (o.cluster_split >= 0) opts.cluster_split = o.cluster_split;
         if (o.raster_group >= 0) opts.raster_group = o.raster_group;
         if (o.swap_ab >= 0) opts.swap_ab = o.swap_ab;
+        if (o.multicast >= 0) opts.multicast = o.multicast;
         Selection sel;
         if (select_config(plan->num_sms, pairs, quads, M, N, K, opts, plan->workspace_bytes, &sel) != BWGEMM_OK)
             continue;

@@ -109,15 +109,6 @@ static_assert(sizeof(kFns) / sizeof(kFns[0]) == kNumVariants, "variant tables ou
 
 }  // namespace
 
-int find_variant(int cg, int bn, bool trans, int mc, int ks, bool rs)
-{
-    for (int i = 0; i < kNumVariants; ++i)
-        if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans &&
-            kVariants[i].mc == mc && kVariants[i].ks == ks && kVariants[i].rs == rs)
-            return i;
-    return -1;
-}
-
 int variant_smem_bytes(int idx) { return (idx >= 0 && idx < kNumVariants) ? kFns[idx].smem_bytes : 0; }
 
 cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,

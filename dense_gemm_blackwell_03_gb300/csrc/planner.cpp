@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "tuned_table.h"
 
 namespace bwgemm {
 
@@ -13,17 +14,62 @@ namespace {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The entry of the tuned-options table for this shape, applied to `opts` when
+// the caller allows it and left automatic every option the entry sets.
+bool apply_tuned_table(bwgemm_plan_options_t& opts, int64_t M, int64_t N, int64_t K)
+{
+    if (opts.tuned_table != 0)
+        return false;
+    for (const TunedEntry& e : kTunedTable) {
+        if (e.M == 0)
+            break;
+        if (e.M != M || e.N != N || e.K != K)
+            continue;
+        const int32_t set[] = {e.variant, e.tile_n, e.split_k, e.schedule, e.copy_kblocks,
+                               e.cluster_split, e.raster_group, e.swap_ab, e.multicast};
+        const int32_t mine[] = {opts.variant, opts.tile_n, opts.split_k, opts.schedule, opts.copy_kblocks,
+                                opts.cluster_split, opts.raster_group, opts.swap_ab, opts.multicast};
+        for (int i = 0; i < 9; ++i)
+            if (set[i] != 0 && mine[i] != 0)
+                return false;  // the caller chose this option itself
+        opts.variant = e.variant ? e.variant : opts.variant;
+        opts.tile_n = e.tile_n ? e.tile_n : opts.tile_n;
+        opts.split_k = e.split_k ? e.split_k : opts.split_k;
+        opts.schedule = e.schedule ? e.schedule : opts.schedule;
+        opts.copy_kblocks = e.copy_kblocks ? e.copy_kblocks : opts.copy_kblocks;
+        opts.cluster_split = e.cluster_split ? e.cluster_split : opts.cluster_split;
+        opts.raster_group = e.raster_group ? e.raster_group : opts.raster_group;
+        opts.swap_ab = e.swap_ab ? e.swap_ab : opts.swap_ab;
+        opts.multicast = e.multicast ? e.multicast : opts.multicast;
+        return true;
+    }
+    return false;
+}
+
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
+int find_variant(int cg, int bn, bool trans, int mc, int ks, bool rs)
+{
+    for (int i = 0; i < kNumVariants; ++i)
+        if (kVariants[i].cg == cg && kVariants[i].bn == bn && kVariants[i].trans == trans &&
+            kVariants[i].mc == mc && kVariants[i].ks == ks && kVariants[i].rs == rs)
+            return i;
+    return -1;
+}
+
 bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t M, int64_t N,
-                              int64_t K, const bwgemm_plan_options_t& opts,
+                              int64_t K, const bwgemm_plan_options_t& opts_in,
                               uint64_t workspace_bytes, Selection* out)
 {
     if (!out || num_sms <= 0 || M < 0 || N < 0 || K < 0)
         return BWGEMM_ERR_INVALID_ARG;
+    if (opts_in.tuned_table < 0 || opts_in.tuned_table > 1)
+        return BWGEMM_ERR_INVALID_ARG;
+    bwgemm_plan_options_t opts = opts_in;
+    const bool tuned = apply_tuned_table(opts, M, N, K);
     if (max_pairs <= 0)
         max_pairs = num_sms / 2;
     if (max_quads <= 0)
@@ -289,6 +335,7 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.swap_ab = swap ? 1 : 0;
     sel.cfg.multicast = mc;
     sel.cfg.cluster_split = cluster_split ? 1 : 0;
+    sel.cfg.tuned = tuned ? 1 : 0;
     // K blocks per operand copy.  Two (3-D copies) when the kernel is compute
     // bound: one TMA copy occupies its unit for ~140 ns whatever its size, and
     // two 16 KiB copies per K block take longer than the K block's MMAs.  In

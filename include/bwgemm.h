@@ -115,7 +115,11 @@ typedef struct {
                                  one-wave split-K tile run in one cluster and exchange
                                  partials through distributed shared memory (when a
                                  cluster per tile fits at once)                          */
-    int32_t reserved[2];      /* must be zero                                            */
+    int32_t tuned_table;      /* 0 = apply the library's table of tuned options when the
+                                 shape matches one of its entries exactly and every
+                                 option the entry sets is left automatic, 1 = plan
+                                 from the rules alone                                   */
+    int32_t reserved[1];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
 /* The launch configuration chosen for a shape (for inspection and tests). */
@@ -149,6 +153,7 @@ typedef struct {
     int32_t prefetch_b;   /* the streamed operand: 1 = B (the kernel's), 0 = A   */
     int32_t cluster_split; /* 1: split_k = 2 slices per tile inside one cluster,
                               partials exchanged in distributed shared memory    */
+    int32_t tuned;         /* 1: an entry of the tuned-options table was applied */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */
@@ -324,6 +329,11 @@ bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, int32_t sourc
  * chosen configuration's result (every candidate computes the same C).
  * Synchronises `stream`.  *best (may be NULL) receives the chosen
  * configuration.  Not thread-safe with other calls on the same plan.
+ * The timing is back to back on the caller's operands, which stay in L2
+ * when they are smaller than it: the choice is the fastest for multiplying
+ * those operands repeatedly, not necessarily for operands streamed from HBM.
+ * (The library's own table of tuned options comes from a sweep that
+ * re-times each choice in steady state on rotated inputs.)
  */
 bwgemm_status_t bwgemm_tune(bwgemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
                             int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,

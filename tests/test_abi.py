@@ -447,3 +447,67 @@ def test_bench_load_path_rejects_bad_arguments(lib):
         assert lib.bwgemm_bench_load_path(0, layout, source, ctas, stages, kblocks, ctypes.byref(gbs),
                                           ctypes.byref(ms)) == INVALID
     assert lib.bwgemm_bench_load_path(0, 0, 0, 0, 6, 64, None, ctypes.byref(ms)) == INVALID
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+def test_tuned_table_entries_apply(tmp_path):
+    """The planner's table lookup (csrc/planner.cpp) compiled on the host with a
+    substitute table of one entry: the entry applies to its exact shape when
+    the options it sets are automatic, not when the caller set one of them,
+    not with tuned_table = 1, and not to other shapes."""
+    csrc = os.path.join(ROOT, "dense_gemm_blackwell_03_gb300", "csrc")
+    cuda_inc = "/usr/local/cuda/include"
+    if not os.path.exists(os.path.join(cuda_inc, "cuda.h")):
+        pytest.skip("needs the CUDA headers")
+    table = tmp_path / "tuned_table.h"
+    table.write_text(
+        "#pragma once\n#include <cstdint>\nnamespace bwgemm {\n"
+        "struct TunedEntry { int64_t M, N, K; int32_t variant, tile_n, split_k, schedule, copy_kblocks,"
+        " cluster_split, raster_group, swap_ab, multicast; };\n"
+        "constexpr TunedEntry kTunedTable[] = {\n"
+        "  {4096, 4096, 4096, 2, 224, 0, 0, 0, 0, 4, 1, 0},\n"
+        "  {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},\n};\n}\n")
+    main = tmp_path / "main.cpp"
+    main.write_text(
+        '#include <cstdio>\n#include "bwgemm.h"\n'
+        "static void show(int64_t M, int table, int tile) {\n"
+        "  bwgemm_plan_options_t o; bwgemm_default_options(&o); o.tuned_table = table; o.tile_n = tile;\n"
+        "  bwgemm_config_t c; int st = bwgemm_select_config(148, 74, 36, M, 4096, 4096, BWGEMM_BF16, &o, &c);\n"
+        '  printf("%d %d %d %d\\n", st, c.tile_n, c.raster_group, c.tuned);\n}\n'
+        "int main() { show(4096, 0, 0); show(4096, 1, 0); show(4096, 0, 256); show(4000, 0, 0); return 0; }\n")
+    # a copy of planner.cpp beside the substitute table (a quoted include looks
+    # in the including file's own directory first)
+    shutil.copy(os.path.join(csrc, "planner.cpp"), tmp_path / "planner.cpp")
+    exe = tmp_path / "planner_test"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", csrc, "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, str(tmp_path / "planner.cpp"), str(main), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = [tuple(int(x) for x in line.split())
+           for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()]
+    assert got[0] == (0, 224, 4, 1)     # the entry: tile 224, raster group 4
+    assert got[1][1:] == (256, 8, 0)    # rules only
+    assert got[2][1:] == (256, 8, 0)    # the caller set tile_n: the entry does not apply
+    assert got[3][3] == 0               # another shape
+
+
+def test_tune_table_header_and_options():
+    from dense_gemm_blackwell_03_gb300 import tune_table
+    rows = [
+        {"shape": "a", "M": 256, "N": 8192, "K": 8192, "gain": 1.03, "rules_us": 32.0, "tuned_us": 31.07,
+         "options": {"variant": 2, "tile_n": 224, "split_k": 2, "schedule": 1, "copy_kblocks": 1,
+                     "cluster_split": 1, "raster_group": 1, "swap_ab": 1, "multicast": 1}},
+        {"shape": "b", "M": 1, "N": 8192, "K": 8192, "gain": 1.005, "rules_us": 27.0, "tuned_us": 26.9,
+         "options": {"variant": 1, "tile_n": 64, "split_k": 2, "schedule": 1, "copy_kblocks": 1,
+                     "cluster_split": 2, "raster_group": 4, "swap_ab": 2, "multicast": 1}},
+        {"shape": "c", "M": 4096, "N": 4096, "K": 4096, "gain": 1.0, "same": True, "options": None},
+    ]
+    text = tune_table.header_text(rows)
+    assert "{256, 8192, 8192, 2, 224, 2, 1, 1, 1, 1, 1, 1},  // a:" in text
+    assert "{1, 8192, 8192" not in text and "{4096" not in text  # below the gain bar / same
+    assert text.rstrip().endswith("}  // namespace bwgemm")
+    # the options that reproduce a configuration, checked through the host planner
+    for M, N, K in ((256, 8192, 8192), (16, 8192, 8192), (4096, 4096, 4096), (512, 8192, 5376)):
+        cfg = binding.select_config(148, M, N, K, max_pairs=74, max_quads=36)
+        again = binding.select_config(148, M, N, K, max_pairs=74, max_quads=36, tuned_table=1,
+                                      **tune_table.options_of(cfg))
+        assert tune_table.same_config(cfg, again), (M, N, K)

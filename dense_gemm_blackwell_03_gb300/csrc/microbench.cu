@@ -28,6 +28,15 @@
 //      the A tile (box {64, 64}) with cluster multicast into both CTAs and
 //      its own B tile (box {64, 128}); every CTA still receives 32 KiB per
 //      K block but issues 24 KiB (the GEMM's multicast of a shared operand).
+//   5  128B swizzle, two K blocks of one 128-row block per copy (a 3-D view,
+//      box {64, 128, 2}: 256 contiguous bytes of every row): a stage holds
+//      two K blocks of A only, so each row is read in 256-byte pieces.
+//   6  128B swizzle, 64 KiB stages of two K blocks of A and B (3-D view),
+//      clusters of two CTAs sharing A: each CTA copies half of A's rows
+//      (box {64, 64, 2}, 16 KiB) with cluster multicast into both CTAs and
+//      its own B (box {64, 128, 2}, 32 KiB); 64 KiB landed, 48 KiB issued.
+//   7  the same 64 KiB stages without multicast: A (box {64, 128, 2}) and B
+//      (box {64, 128, 2}), 64 KiB landed and issued per stage.
 //
 // Every wait is bounded; a run whose waits run out reports BWGEMM_ERR_TIMEOUT
 // after draining the copies it armed.
@@ -62,7 +71,7 @@ struct LoadPathParams {
 
 __global__ void __launch_bounds__(kLpThreads, 1)
     load_path_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap map2,
-                     const LoadPathParams p)
+                     const __grid_constant__ CUtensorMap map3, const LoadPathParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -76,7 +85,10 @@ __global__ void __launch_bounds__(kLpThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    const bool mc = p.layout == 4;  // launched in clusters of two CTAs
+    const bool mc = p.layout == 4 || p.layout == 6;  // launched in clusters of two CTAs
+    // layouts 6 and 7 use stages of two K blocks (64 KiB): half as many
+    const bool big = p.layout >= 6;
+    const uint32_t stage_bytes = big ? 2u * kLpStageBytes : uint32_t(kLpStageBytes);
     const uint32_t rank = mc ? ptx::cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
@@ -119,13 +131,26 @@ __global__ void __launch_bounds__(kLpThreads, 1)
             armed_parity = (armed_parity & ~(1u << s)) | (phase << s);
             if (ptx::elect_one()) {
                 const uint32_t fb = bar_full + 8 * s;
-                const uint32_t dA = ring + uint32_t(s * kLpStageBytes);
-                const uint32_t dB = dA + kLpTileBytes;
+                const uint32_t dA = ring + uint32_t(s) * stage_bytes;
+                const uint32_t dB = dA + (big ? 2u : 1u) * uint32_t(kLpTileBytes);
                 const int kx = ((i + int(blockIdx.x)) % p.src_kblocks) * kTileK;
-                ptx::mbar_arrive_expect_tx(fb, kLpStageBytes);
-                if (p.layout == 3) {
+                ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+                if (big) {
+                    // K blocks 2i and 2i + 1 of A's and of B's rows
+                    const int kc = ((2 * i + 2 * int(blockIdx.x)) % p.src_kblocks);
+                    if (mc)
+                        ptx::tma_load_3d_multicast(dA + rank * uint32_t(kLpTileBytes), &map2, fb, 0,
+                                                   a_row + int(rank) * (kRowsPerCta / 2), kc, uint16_t(0x3u));
+                    else
+                        ptx::tma_load_3d(dA, &map2, fb, 0, a_row, kc);
+                    ptx::tma_load_3d(dB, &map3, fb, 0, b_row, kc);
+                } else if (p.layout == 3) {
                     // A's and B's 128-row blocks as one 256-row box
                     ptx::tma_load_2d(dA, &map2, fb, kx, a_row);
+                } else if (p.layout == 5) {
+                    // K blocks 2i and 2i + 1 of the A rows
+                    const int kc = ((2 * i + 2 * int(blockIdx.x)) % p.src_kblocks);
+                    ptx::tma_load_3d(dA, &map2, fb, 0, a_row, kc);
                 } else if (p.layout == 4) {
                     // this CTA's half of the shared A tile into both CTAs, its own B
                     ptx::tma_load_2d_multicast(dA + rank * uint32_t(kLpTileBytes / 2), &map2, fb, kx,
@@ -209,9 +234,10 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
                                                   int32_t stages, int32_t kblocks, double* gbytes_per_s,
                                                   double* ms)
 {
-    if (!gbytes_per_s || !ms || layout < 0 || layout > 4 || source < 0 || source > 1 || ctas < 0 ||
-        stages < 1 || stages > kLpMaxStages || kblocks < 1 || kblocks > (1 << 20))
-        return BWGEMM_ERR_INVALID_ARG;
+    if (!gbytes_per_s || !ms || layout < 0 || layout > 7 || source < 0 || source > 1 || ctas < 0 ||
+        stages < 1 || stages > kLpMaxStages || kblocks < 1 || kblocks > (1 << 20) ||
+        (layout >= 6 && stages > kLpMaxStages / 2))
+        return BWGEMM_ERR_INVALID_ARG;  // (layouts 6, 7: stages of two K blocks, at most 3)
     int prev = 0;
     if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
         cudaGetLastError();
@@ -223,14 +249,15 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     const int rows = kLpSrcRows[source], cols = kLpSrcCols[source];
     const size_t src_bytes = size_t(rows) * size_t(cols) * 2;
-    // clusters of two CTAs for layout 4: an even number of CTAs
-    const int grid = (ctas > 0 ? ctas : sms) & (layout == 4 ? ~1 : ~0);
+    // clusters of two CTAs for layouts 4 and 6: an even number of CTAs
+    const bool clustered = layout == 4 || layout == 6;
+    const int grid = (ctas > 0 ? ctas : sms) & (clustered ? ~1 : ~0);
     bwgemm_status_t st = BWGEMM_OK;
     void* src = nullptr;
     uint32_t* d_status = nullptr;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     EncodeTiledFn enc = lp_encode_fn();
-    CUtensorMap map, map2;
+    CUtensorMap map, map2, map3;
     if (major != 10 || minor != 3 || sms <= 0) {
         st = BWGEMM_ERR_UNSUPPORTED;
     } else if (grid > sms || grid < 1) {
@@ -253,12 +280,26 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
         // second map: the 256-row box of layout 3, the 64-row half of layout 4
         const cuuint32_t box2[2] = {uint32_t(kTileK), uint32_t(layout == 3 ? 2 * kRowsPerCta : kRowsPerCta / 2)};
         const bool swz = layout == 0 || layout >= 3;
+        // layout 5: the 3-D view {64-element chunk, rows, chunks}, box {64, 128, 2}
+        const cuuint64_t dims3[3] = {cuuint64_t(kTileK), cuuint64_t(rows), cuuint64_t(cols / kTileK)};
+        const cuuint64_t strides3[2] = {cuuint64_t(cols) * 2, cuuint64_t(kTileK) * 2};
+        // layout 6: A's halves ({64, 64, 2}) in map2, B's whole rows ({64, 128, 2}) in map3
+        const cuuint32_t box3[3] = {uint32_t(kTileK), uint32_t(layout == 6 ? kRowsPerCta / 2 : kRowsPerCta), 2};
+        const cuuint32_t box3b[3] = {uint32_t(kTileK), uint32_t(kRowsPerCta), 2};
+        const cuuint32_t estr3[3] = {1, 1, 1};
         if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-            enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box2, estr,
+            enc(&map3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims3, strides3, box3b, estr3,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            (layout >= 5 ? enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, src, dims3, strides3, box3, estr3,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)
+                         : enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, src, dims, strides, box2, estr,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)) !=
+                CUDA_SUCCESS)
             st = BWGEMM_ERR_CUDA;
     }
     if (st == BWGEMM_OK) {
@@ -276,15 +317,15 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
         cfg.dynamicSmemBytes = kLpSmem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = layout == 4 ? 2 : 1;
+        attr[0].val.clusterDim.x = clustered ? 2 : 1;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         // a warm-up launch (tensor map; the L2 source filled), then the timed one
-        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, p);
+        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, map3, p);
         cudaEventRecord(e0);
-        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, p);
+        cudaLaunchKernelEx(&cfg, load_path_kernel, map, map2, map3, p);
         cudaEventRecord(e1);
         uint32_t h_status = 0;
         float t = 0.f;
@@ -298,7 +339,8 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
             st = BWGEMM_ERR_CUDA;
         else {
             *ms = double(t);
-            *gbytes_per_s = double(grid) * double(kblocks) * double(kLpStageBytes) / (double(t) * 1e-3) / 1e9;
+            const double stage = double(layout >= 6 ? 2 * kLpStageBytes : kLpStageBytes);
+            *gbytes_per_s = double(grid) * double(kblocks) * stage / (double(t) * 1e-3) / 1e9;
         }
     }
     if (e0)

@@ -246,6 +246,17 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
         : "memory");
 }
 
+// 3-D form of tma_load_2d_multicast.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                      int32_t c0, int32_t c1, int32_t c2, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
+        : "memory");
+}
+
 // Prefetch one 2-D box of a tensor into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1)
 {

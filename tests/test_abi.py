@@ -441,7 +441,7 @@ def test_noalloc_scratch_stays_inside_the_array(lib):
 def test_bench_load_path_rejects_bad_arguments(lib):
     # argument checks come before any device access (no GPU needed)
     gbs, ms = ctypes.c_double(), ctypes.c_double()
-    for layout, source, ctas, stages, kblocks in ((5, 0, 0, 6, 64), (-1, 0, 0, 6, 64), (0, 2, 0, 6, 64),
+    for layout, source, ctas, stages, kblocks in ((8, 0, 0, 6, 64), (6, 0, 0, 4, 64), (-1, 0, 0, 6, 64), (0, 2, 0, 6, 64),
                                                   (0, -1, 0, 6, 64), (0, 0, -1, 6, 64), (0, 0, 0, 0, 64),
                                                   (0, 0, 0, 7, 64), (0, 0, 0, 6, 0)):
         assert lib.bwgemm_bench_load_path(0, layout, source, ctas, stages, kblocks, ctypes.byref(gbs),
@@ -485,8 +485,8 @@ def test_tuned_table_entries_apply(tmp_path):
     got = [tuple(int(x) for x in line.split())
            for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()]
     assert got[0] == (0, 224, 4, 1)     # the entry: tile 224, raster group 4
-    assert got[1][1:] == (256, 8, 0)    # rules only
-    assert got[2][1:] == (256, 8, 0)    # the caller set tile_n: the entry does not apply
+    assert got[1][1:] == (256, 16, 0)   # rules only (4096^3: every row block of a column first)
+    assert got[2][1:] == (256, 16, 0)   # the caller set tile_n: the entry does not apply
     assert got[3][3] == 0               # another shape
 
 
@@ -511,3 +511,14 @@ def test_tune_table_header_and_options():
         again = binding.select_config(148, M, N, K, max_pairs=74, max_quads=36, tuned_table=1,
                                       **tune_table.options_of(cfg))
         assert tune_table.same_config(cfg, again), (M, N, K)
+
+
+def test_select_raster_group_by_operand_size():
+    # operands within half the L2: walk every row block of a column first;
+    # larger ones: groups of 8 row blocks
+    assert binding.select_config(148, 4096, 4096, 4096, max_pairs=74)["raster_group"] == 16
+    assert binding.select_config(148, 8192, 8192, 8192, max_pairs=74)["raster_group"] == 8
+    assert binding.select_config(148, 8192, 28672, 8192, max_pairs=74)["raster_group"] == 8
+    assert binding.select_config(148, 2048, 2048, 2048, max_pairs=74)["raster_group"] == 8  # 8 row blocks
+    assert binding.select_config(148, 4096, 4096, 4096, max_pairs=74, raster_group=4)["raster_group"] == 4
+

@@ -44,7 +44,10 @@ EXPORTED = [
 LOAD_PATH_LAYOUTS = {0: "128B swizzle", 1: "no swizzle, plain rows (same copies)",
                      2: "no swizzle, interleaved core matrices (8 copies per tile)",
                      3: "128B swizzle, one 256-row copy per K block",
-                     4: "128B swizzle, A multicast in halves across two CTAs"}
+                     4: "128B swizzle, A multicast in halves across two CTAs",
+                     5: "128B swizzle, two K blocks (256-byte row pieces) per copy",
+                     6: "128B swizzle, 64 KiB stages, A multicast in halves across two CTAs",
+                     7: "128B swizzle, 64 KiB stages, no multicast"}
 
 # timeline slots of bwgemm_plan_read_trace
 (TRACE_ENTRY, TRACE_READY, TRACE_FIRST_LOAD, TRACE_LAST_LOAD, TRACE_EPI_DONE, TRACE_EXIT, TRACE_SETUP,

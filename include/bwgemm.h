@@ -302,7 +302,14 @@ bwgemm_status_t bwgemm_probe_tensor_rate(int device, double* flop_per_clock_per_
  * (the same bytes in half the copies), 4 = 128B swizzle in clusters of two
  * CTAs that share A: each copies half of the A tile with cluster multicast
  * into both and its own B tile (the same bytes landed, three quarters
- * issued; an even number of CTAs).  Writes the bytes landed by all CTAs per second (GB/s, one
+ * issued; an even number of CTAs), 5 = 128B swizzle, two K blocks of one
+ * 128-row block per copy (box {64, 128, 2} of a 3-D view: 256 contiguous
+ * bytes of each row; A only), 6 = 128B swizzle, stages of two K blocks of
+ * A and B (64 KiB, `stages` at most 3) in clusters of two CTAs sharing A:
+ * each copies half of A's rows (box {64, 64, 2}) with cluster multicast and
+ * its own B (box {64, 128, 2}), 7 = the same stages without multicast.  For
+ * layouts 6 and 7 `kblocks` counts stages of two K blocks.  Writes the
+ * bytes landed by all CTAs per second (GB/s, one
  * timed launch after a warm-up launch, CUDA events) to *gbytes_per_s and the
  * launch's time to *ms.  Allocates and frees its source matrix; synchronises
  * the device.  Errors: BWGEMM_ERR_INVALID_ARG (NULL output or an argument

@@ -11,8 +11,12 @@ reported under "shapes".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timing: CUDA events on the launching stream, W untimed warm-up steps, then K
-steps bracketed by a device synchronisation on both sides.  Inputs rotate
+Timing: CUDA events on the launching stream.  The GPU idles ``--idle``
+seconds, then W untimed warm-up steps run straight into the K timed steps,
+which are bracketed by a device synchronisation on both sides (so every box
+starts the timed region from the same state; cuBLAS's context figure is timed
+the same way).  ``value`` is the K steps' mean; ``median_ms`` is the median of
+at least 50 separately event-timed launches.  Inputs rotate
 over enough copies that their total exceeds twice the L2 (129 MB), so no step
 reads operands left in L2 by the step before.  The library runs on one GPU
 and has no multi-GPU path: ``--gpus`` other than 1 is refused.
@@ -361,13 +365,17 @@ def run_ours(args):
         plan.gemm(A, B, out=C, stream=stream)
 
     sets = input_sets(shape, device, l2_bytes)
+    ours(*sets[0])  # the plan's tensor maps and the module, set up outside the region
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # Every box starts from the same state: the GPU idles, then the W warm-up
+    # steps run straight into the K timed ones (cuBLAS below the same way).
+    time.sleep(args.idle)
     for i in range(args.warmup):
         ours(*sets[i % len(sets)])
     torch.cuda.synchronize()
     n0 = plan.launch_count()
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
     sampler.begin()
     total_ms = time_region(ours, sets, args.steps, 0, stream)
     sampler.end()
@@ -401,7 +409,9 @@ def run_ours(args):
     # cuBLAS (torch.matmul) on the same tensors, as same-box context
     def cublas(A, B, C):
         torch.matmul(A, B.t(), out=C)
-    cb_ms = time_region(cublas, sets, args.steps, 5, stream)
+    torch.cuda.synchronize()
+    time.sleep(args.idle)
+    cb_ms = time_region(cublas, sets, args.steps, args.warmup, stream)
     cb_s = cb_ms / 1e3 / args.steps
 
     # end-to-end through the C ABI with host buffers (H2D of A, B and D2H of C each step)
@@ -560,6 +570,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--idle", type=float, default=2.0,
+                    help="idle seconds before the headline's warm-up steps (and cuBLAS's)")
     ap.add_argument("--cooldown", type=float, default=1.0,
                     help="idle seconds before each extra shape (ours and cuBLAS alike)")
     ap.add_argument("--shape-warmup", type=float, default=1.0,

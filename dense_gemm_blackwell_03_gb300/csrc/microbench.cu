@@ -37,6 +37,9 @@
 //      its own B (box {64, 128, 2}, 32 KiB); 64 KiB landed, 48 KiB issued.
 //   7  the same 64 KiB stages without multicast: A (box {64, 128, 2}) and B
 //      (box {64, 128, 2}), 64 KiB landed and issued per stage.
+//   8  the same 64 KiB stages, clusters of two CTAs sharing both tiles whole:
+//      rank 0 copies A (box {64, 128, 2}) with multicast into both CTAs,
+//      rank 1 copies B the same way; 64 KiB landed, 32 KiB issued per CTA.
 //
 // Every wait is bounded; a run whose waits run out reports BWGEMM_ERR_TIMEOUT
 // after draining the copies it armed.
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kLpThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    const bool mc = p.layout == 4 || p.layout == 6;  // launched in clusters of two CTAs
+    const bool mc = p.layout == 4 || p.layout == 6 || p.layout == 8;  // clusters of two CTAs
     // layouts 6 and 7 use stages of two K blocks (64 KiB): half as many
     const bool big = p.layout >= 6;
     const uint32_t stage_bytes = big ? 2u * kLpStageBytes : uint32_t(kLpStageBytes);
@@ -138,12 +141,20 @@ __global__ void __launch_bounds__(kLpThreads, 1)
                 if (big) {
                     // K blocks 2i and 2i + 1 of A's and of B's rows
                     const int kc = ((2 * i + 2 * int(blockIdx.x)) % p.src_kblocks);
-                    if (mc)
-                        ptx::tma_load_3d_multicast(dA + rank * uint32_t(kLpTileBytes), &map2, fb, 0,
-                                                   a_row + int(rank) * (kRowsPerCta / 2), kc, uint16_t(0x3u));
-                    else
-                        ptx::tma_load_3d(dA, &map2, fb, 0, a_row, kc);
-                    ptx::tma_load_3d(dB, &map3, fb, 0, b_row, kc);
+                    if (p.layout == 8) {
+                        // whole tiles: rank 0 brings A, rank 1 brings B, each into both CTAs
+                        if (rank == 0)
+                            ptx::tma_load_3d_multicast(dA, &map3, fb, 0, a_row, kc, uint16_t(0x3u));
+                        else
+                            ptx::tma_load_3d_multicast(dB, &map3, fb, 0, b_row, kc, uint16_t(0x3u));
+                    } else {
+                        if (mc)
+                            ptx::tma_load_3d_multicast(dA + rank * uint32_t(kLpTileBytes), &map2, fb, 0,
+                                                       a_row + int(rank) * (kRowsPerCta / 2), kc, uint16_t(0x3u));
+                        else
+                            ptx::tma_load_3d(dA, &map2, fb, 0, a_row, kc);
+                        ptx::tma_load_3d(dB, &map3, fb, 0, b_row, kc);
+                    }
                 } else if (p.layout == 3) {
                     // A's and B's 128-row blocks as one 256-row box
                     ptx::tma_load_2d(dA, &map2, fb, kx, a_row);
@@ -234,7 +245,7 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
                                                   int32_t stages, int32_t kblocks, double* gbytes_per_s,
                                                   double* ms)
 {
-    if (!gbytes_per_s || !ms || layout < 0 || layout > 7 || source < 0 || source > 1 || ctas < 0 ||
+    if (!gbytes_per_s || !ms || layout < 0 || layout > 8 || source < 0 || source > 1 || ctas < 0 ||
         stages < 1 || stages > kLpMaxStages || kblocks < 1 || kblocks > (1 << 20) ||
         (layout >= 6 && stages > kLpMaxStages / 2))
         return BWGEMM_ERR_INVALID_ARG;  // (layouts 6, 7: stages of two K blocks, at most 3)
@@ -250,7 +261,7 @@ extern "C" bwgemm_status_t bwgemm_bench_load_path(int device, int32_t layout, in
     const int rows = kLpSrcRows[source], cols = kLpSrcCols[source];
     const size_t src_bytes = size_t(rows) * size_t(cols) * 2;
     // clusters of two CTAs for layouts 4 and 6: an even number of CTAs
-    const bool clustered = layout == 4 || layout == 6;
+    const bool clustered = layout == 4 || layout == 6 || layout == 8;
     const int grid = (ctas > 0 ? ctas : sms) & (clustered ? ~1 : ~0);
     bwgemm_status_t st = BWGEMM_OK;
     void* src = nullptr;

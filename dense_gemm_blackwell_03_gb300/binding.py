@@ -82,6 +82,7 @@ class PlanOptions(ctypes.Structure):
         ("copy_kblocks", ctypes.c_int32),
         ("cluster_split", ctypes.c_int32),
         ("tuned_table", ctypes.c_int32),
+        ("skinny", ctypes.c_int32),
         ("reserved", ctypes.c_int32 * 1),
     ]
 
@@ -111,6 +112,7 @@ class Config(ctypes.Structure):
         ("prefetch_b", ctypes.c_int32),
         ("cluster_split", ctypes.c_int32),
         ("tuned", ctypes.c_int32),
+        ("skinny", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

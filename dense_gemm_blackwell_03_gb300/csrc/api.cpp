@@ -43,7 +43,7 @@ struct TmapSlot {
     int64_t inner = 0, outer = 0, ld = 0;
     int64_t chunks = 0;  // 3-D K-chunk views: number of whole 64-element chunks (0: 2-D map)
     int dtype = -1;
-    uint32_t box_inner = 0, box_outer = 0;
+    uint32_t box_inner = 0, box_outer = 0, box_depth = 0;
     int swizzle = -1;
     bool valid = false;
     CUtensorMap map;
@@ -87,23 +87,24 @@ bwgemm_status_t get_tmap(TmapSlot& s, const void* ptr, int dtype, int64_t inner,
     return BWGEMM_OK;
 }
 
-// Build (or reuse) a 3-D view of a K-major operand for copies of two K blocks
-// at once: dimension 0 = the 64 elements of one K chunk, 1 = rows (ld apart),
-// 2 = whole K chunks (128 bytes apart).  A box {64, box_rows, 2} lands as two
-// consecutive 128-byte-swizzled [box_rows x 64] blocks, i.e. two adjacent ring
-// stages.  Only whole chunks are described, so no copy reads past K.
+// Build (or reuse) a 3-D view of a K-major operand for copies of several K
+// blocks at once: dimension 0 = the 64 elements of one K chunk, 1 = rows (ld
+// apart), 2 = whole K chunks (128 bytes apart).  A box {64, box_rows, depth}
+// lands as `depth` consecutive 128-byte-swizzled [box_rows x 64] blocks (for
+// the main kernel depth 2: two adjacent ring stages).  Only whole chunks are
+// described, so no copy reads past K.
 bwgemm_status_t get_tmap3(TmapSlot& s, const void* ptr, int dtype, int64_t chunks, int64_t rows,
-                          int64_t ld, uint32_t box_rows)
+                          int64_t ld, uint32_t box_rows, uint32_t depth = 2)
 {
     if (s.valid && s.chunks == chunks && s.ptr == ptr && s.outer == rows && s.ld == ld &&
-        s.dtype == dtype && s.box_outer == box_rows)
+        s.dtype == dtype && s.box_outer == box_rows && s.box_depth == depth)
         return BWGEMM_OK;
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return BWGEMM_ERR_NO_DEVICE;
     const cuuint64_t dims[3] = {cuuint64_t(kTileK), cuuint64_t(rows), cuuint64_t(chunks)};
     const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, cuuint64_t(kTileK) * 2};
-    const cuuint32_t box[3] = {uint32_t(kTileK), box_rows, 2};
+    const cuuint32_t box[3] = {uint32_t(kTileK), box_rows, depth};
     const cuuint32_t estr[3] = {1, 1, 1};
     s.valid = false;
     const CUresult r = enc(&s.map,
@@ -122,6 +123,7 @@ bwgemm_status_t get_tmap3(TmapSlot& s, const void* ptr, int dtype, int64_t chunk
     s.dtype = dtype;
     s.box_inner = kTileK;
     s.box_outer = box_rows;
+    s.box_depth = depth;
     s.swizzle = int(CU_TENSOR_MAP_SWIZZLE_128B);
     s.valid = true;
     return BWGEMM_OK;
@@ -249,6 +251,59 @@ const bwgemm_plan_options_t& options_for(bwgemm_plan_t plan, int64_t M, int64_t 
     return plan->opts;
 }
 
+// The whole-K kernel for a few rows of A: the weights (B, N x K) are the MMA's
+// A operand in 64-row boxes, A's rows its B operand in boxes of skinny_bn /
+// skinny_cg rows (zero-filled past M: each CTA of a pair copies its half);
+// 3-D views copy skinny_kblocks(bn) whole K chunks at once.  C is stored in
+// boxes of bn / cg rows x 16 cg columns (clipped at M and N).
+bwgemm_status_t enqueue_skinny(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, const Selection& sel,
+                               const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, cudaStream_t stream)
+{
+    bwgemm_status_t st;
+    const uint32_t bn = uint32_t(sel.skinny_bn);
+    const uint32_t cg = uint32_t(skinny_cg(int(bn)));
+    const uint32_t x_rows = bn / cg;
+    if ((st = get_tmap(plan->tmaps[0], B, dtype, K, N, ldb, kTileK, uint32_t(kSkinnyRows),
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != BWGEMM_OK ||
+        (st = get_tmap(plan->tmaps[1], A, dtype, K, M, lda, kTileK, x_rows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            BWGEMM_OK)
+        return st;
+    if ((st = get_tmap(plan->tmaps[2], C, dtype, N, M, ldc, 16 * cg, x_rows, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+        BWGEMM_OK)
+        return st;
+    GemmParams p = make_params(sel, M, N, K, dtype);
+    const int64_t chunks = K / kTileK;
+    const int kps = skinny_kblocks(int(bn));
+    const bool views = chunks >= kps;
+    const uint32_t depth = uint32_t(kps);
+    if (views &&
+        ((st = get_tmap3(plan->tmaps[3], B, dtype, chunks, N, ldb, uint32_t(kSkinnyRows), depth)) != BWGEMM_OK ||
+         (st = get_tmap3(plan->tmaps[4], A, dtype, chunks, M, lda, x_rows, depth)) != BWGEMM_OK))
+        return st;
+    p.k_chunks_a = views ? int32_t(chunks) : 0;
+    p.k_chunks_b = views ? int32_t(chunks) : 0;
+    p.timeout_ns = opts.timeout_ns ? opts.timeout_ns : 4000000000ull;
+    p.status = plan->d_status;
+    p.c = static_cast<uint16_t*>(C);
+    p.ldc = ldc;
+    p.stall_kblock = opts.stall_kblock;
+    if (plan->d_trace) {
+        if (sel.cfg.grid > plan->trace_ctas)
+            return BWGEMM_ERR_UNSUPPORTED;
+        p.trace = plan->d_trace;
+    }
+    const CUtensorMap& w3 = views ? plan->tmaps[3].map : plan->tmaps[0].map;
+    const CUtensorMap& x3 = views ? plan->tmaps[4].map : plan->tmaps[1].map;
+    if (launch_skinny(int(bn), plan->tmaps[0].map, plan->tmaps[1].map, w3, x3, plan->tmaps[2].map, p,
+                      sel.cfg.grid, stream, opts.pdl_off == 0) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    plan->last = sel.cfg;
+    plan->last_grid = sel.cfg.grid;
+    plan->launches += 1;
+    return BWGEMM_OK;
+}
+
 bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, const void* A,
                         const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                         int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, cudaStream_t stream)
@@ -273,6 +328,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, c
                        plan->workspace_bytes, &sel);
     if (st != BWGEMM_OK)
         return st;
+    if (sel.skinny_bn > 0)
+        return enqueue_skinny(plan, opts, sel, A, B, C, M, N, K, lda, ldb, ldc, dtype, stream);
     const Variant& v = kVariants[sel.variant_idx];
     const uint32_t b_rows = uint32_t(v.cg == 1 ? v.bn : v.bn / 2);
     // the MMA's A operand (128-row side) and B operand; exchanged when swapped

@@ -79,12 +79,32 @@ int64_t host_block_rows(int64_t M, int64_t N, int64_t K);
 // this GPU's own memory.
 bwgemm_status_t check_operands_resident(const void* A, const void* B, const void* C, int64_t K, int device);
 
+// The whole-K kernel for decode batches of at most 64 rows of A
+// (skinny_kernel.cuh): 64 weight rows per CTA, the rows of A as the MMA's N
+// (bn = 16, 32 or 64), no split of K.  skinny_cg(bn) CTAs per MMA: at bn =
+// 64 a cluster of two (M = 128, cta_group::2), each CTA copying half of A's
+// rows; one CTA (M = 64) below.  `skinny_stages(bn)` ring stages of
+// `skinny_kblocks(bn)` K blocks in about 200 KiB of shared memory: four K
+// blocks per stage (one 32 KiB copy of the weights) where a CTA copies at
+// most 32 rows of A, two otherwise.
+constexpr int kSkinnyRows = 64;
+constexpr int skinny_cg(int bn) { return bn == 64 ? 2 : 1; }
+constexpr int skinny_kblocks(int bn) { return bn / skinny_cg(bn) <= 32 ? 4 : 2; }
+constexpr int skinny_stages(int bn)
+{
+    return (200 * 1024) / (skinny_kblocks(bn) * (kSkinnyRows + bn / skinny_cg(bn)) * 128);
+}
+cudaError_t launch_skinny(int bn, const CUtensorMap& w, const CUtensorMap& x, const CUtensorMap& w3,
+                          const CUtensorMap& x3, const CUtensorMap& c, const GemmParams& p, int grid,
+                          cudaStream_t stream, bool pdl);
+
 // Sizes of the split-K workspace regions.
 constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) arrival counters
 
 struct Selection {
     bwgemm_config_t cfg;
-    int variant_idx;
+    int variant_idx;  // into kVariants; -1 for the whole-K kernel of skinny_bn > 0
+    int skinny_bn;    // > 0: the whole-K kernel for a few rows of A, MMA N = skinny_bn
     bool swap;  // the kernel sees the problem N x M (A and B exchanged)
     int num_m_blocks, num_n_blocks, num_k_blocks;
     int64_t sk_iters;

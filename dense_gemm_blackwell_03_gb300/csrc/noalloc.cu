@@ -95,6 +95,7 @@ bwgemm_status_t noalloc_select(int num_sms, int max_pairs, int64_t M, int64_t N,
     opts.swap_ab = 1;        // operands in the order given
     opts.multicast = 1;      // one CTA pair per cluster: the scratch below is sized for it
     opts.cluster_split = 1;  // slices reduce through the scratch array, not in a cluster
+    opts.skinny = 1;         // the split-K kernel, also for a few rows of A
     // plan as if the workspace were unbounded, then hold the need against the array
     const bwgemm_status_t st = select_config(num_sms, max_pairs, 0, M, N, K, opts, ~uint64_t(0), sel);
     if (st != BWGEMM_OK)

@@ -26,10 +26,10 @@ bool apply_tuned_table(bwgemm_plan_options_t& opts, int64_t M, int64_t N, int64_
         if (e.M != M || e.N != N || e.K != K)
             continue;
         const int32_t set[] = {e.variant, e.tile_n, e.split_k, e.schedule, e.copy_kblocks,
-                               e.cluster_split, e.raster_group, e.swap_ab, e.multicast};
+                               e.cluster_split, e.raster_group, e.swap_ab, e.multicast, e.skinny};
         const int32_t mine[] = {opts.variant, opts.tile_n, opts.split_k, opts.schedule, opts.copy_kblocks,
-                                opts.cluster_split, opts.raster_group, opts.swap_ab, opts.multicast};
-        for (int i = 0; i < 9; ++i)
+                                opts.cluster_split, opts.raster_group, opts.swap_ab, opts.multicast, opts.skinny};
+        for (int i = 0; i < 10; ++i)
             if (set[i] != 0 && mine[i] != 0)
                 return false;  // the caller chose this option itself
         opts.variant = e.variant ? e.variant : opts.variant;
@@ -41,6 +41,7 @@ bool apply_tuned_table(bwgemm_plan_options_t& opts, int64_t M, int64_t N, int64_
         opts.raster_group = e.raster_group ? e.raster_group : opts.raster_group;
         opts.swap_ab = e.swap_ab ? e.swap_ab : opts.swap_ab;
         opts.multicast = e.multicast ? e.multicast : opts.multicast;
+        opts.skinny = e.skinny ? e.skinny : opts.skinny;
         return true;
     }
     return false;
@@ -140,6 +141,60 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     if (opts.schedule < BWGEMM_SCHEDULE_AUTO || opts.schedule > BWGEMM_SCHEDULE_CLC)
         return BWGEMM_ERR_INVALID_ARG;
     const bool clc = opts.schedule == BWGEMM_SCHEDULE_CLC;
+
+    // Decode batches of at most 64 rows: the whole-K kernel with 64 weight rows
+    // per CTA and the rows of A as the MMA's N, when its CTAs fit one wave: no
+    // split of K, so no partial sums to exchange after the last MMA, which is
+    // what split-K on 128-row tiles pays (N = 8192: 128 CTAs).  More than 32
+    // rows: CTA pairs (M = 128 across the pair), each CTA copying half of A's
+    // rows.  Taken unless an option asks for something only the main kernel
+    // does.
+    if (opts.skinny < 0 || opts.skinny > 2)
+        return BWGEMM_ERR_INVALID_ARG;
+    {
+        const int sbn = Nk <= 16 ? 16 : (Nk <= 32 ? 32 : 64);
+        const int scg = skinny_cg(sbn);
+        const int64_t sk_units = ceil_div(Mk, int64_t(kSkinnyRows) * scg);  // CTAs or pairs
+        const int64_t sk_ctas = sk_units * scg;
+        const bool forced_other = opts.variant != BWGEMM_VARIANT_AUTO || opts.tile_n != 0 || opts.split_k > 1 ||
+                                  clc || opts.schedule == BWGEMM_SCHEDULE_STREAM_K || mc != 1 ||
+                                  opts.cluster_split == 2 || opts.prefetch > 0 || opts.copy_kblocks != 0 ||
+                                  opts.raster_group > 0;
+        const bool fits = swap && Nk <= 64 && sk_units >= 1 && sk_ctas <= num_sms &&
+                          (scg == 1 || sk_units <= max_pairs) && (opts.max_ctas == 0 || sk_ctas <= opts.max_ctas);
+        if (opts.skinny == 2 && !fits)
+            return BWGEMM_ERR_UNSUPPORTED;
+        if (fits && (opts.skinny == 2 || (opts.skinny == 0 && !forced_other))) {
+            Selection sel;
+            std::memset(&sel, 0, sizeof(sel));
+            sel.variant_idx = -1;
+            sel.skinny_bn = sbn;
+            sel.swap = true;
+            sel.num_m_blocks = int(sk_units);
+            sel.num_n_blocks = 1;
+            sel.num_k_blocks = int(num_kb);
+            sel.cfg.variant = scg == 2 ? BWGEMM_VARIANT_2SM : BWGEMM_VARIANT_1SM;
+            sel.cfg.tile_m = kSkinnyRows * scg;
+            sel.cfg.tile_n = sbn;
+            sel.cfg.tile_k = kTileK;
+            sel.cfg.stages = skinny_stages(sbn);
+            sel.cfg.split_k = 1;
+            sel.cfg.raster_group = 1;
+            sel.cfg.num_tiles = int32_t(sk_units);
+            sel.cfg.num_units = int32_t(sk_units);
+            sel.cfg.grid = int32_t(sk_ctas);
+            sel.cfg.schedule = BWGEMM_SCHEDULE_TILES;
+            sel.cfg.dp_tiles = int32_t(sk_units);
+            sel.cfg.workers = int32_t(sk_units);
+            sel.cfg.swap_ab = 1;
+            sel.cfg.multicast = 1;
+            sel.cfg.copy_kblocks = K / kTileK >= skinny_kblocks(sbn) ? skinny_kblocks(sbn) : 1;
+            sel.cfg.tuned = tuned ? 1 : 0;
+            sel.cfg.skinny = 1;
+            *out = sel;
+            return BWGEMM_OK;
+        }
+    }
 
     // Tile width of the pair form: 224, 320 or 384 instead of 256 columns
     // when the problem then fits one wave clearly better.  N = 8192 makes 32
@@ -377,9 +432,28 @@ int64_t host_block_rows(int64_t M, int64_t N, int64_t K)
 
 GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype)
 {
-    const Variant& v = kVariants[sel.variant_idx];
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
+    if (sel.skinny_bn > 0) {
+        // the whole-K kernel: the weight rows (the caller's N) are its M
+        p.M = int32_t(N);
+        p.N = int32_t(M);
+        p.K = int32_t(K);
+        p.num_m_blocks = sel.num_m_blocks;
+        p.num_n_blocks = 1;
+        p.num_k_blocks = sel.num_k_blocks;
+        p.num_tiles = sel.cfg.num_tiles;
+        p.split_k = 1;
+        p.dp_tiles = sel.cfg.num_tiles;
+        p.dp_units = sel.cfg.num_tiles;
+        p.raster_group = 1;
+        p.dtype = int32_t(dtype);
+        p.idesc = make_idesc(int(dtype), kSkinnyRows * skinny_cg(sel.skinny_bn), sel.skinny_bn);
+        p.stall_kblock = -1;
+        p.ks = 1;
+        return p;
+    }
+    const Variant& v = kVariants[sel.variant_idx];
     p.M = int32_t(sel.swap ? N : M);  // the kernel's problem
     p.N = int32_t(sel.swap ? M : N);
     p.K = int32_t(K);

@@ -13,12 +13,12 @@ struct TunedEntry {
     int64_t M, N, K;
     // the options the entry sets (0 = automatic, as in bwgemm_plan_options_t)
     int32_t variant, tile_n, split_k, schedule, copy_kblocks, cluster_split, raster_group, swap_ab,
-        multicast;
+        multicast, skinny;
 };
 
 // the last entry (M = 0) ends the table
 constexpr TunedEntry kTunedTable[] = {
-    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},
 };
 
 }  // namespace bwgemm

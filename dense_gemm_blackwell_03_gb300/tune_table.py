@@ -36,15 +36,17 @@ SWEEP_SHAPES = ["square4096", "prefill_attn_out", "prefill_mlp_up", "decode_attn
                 "tail_m64", "tail_m200"]
 # the plan options a table entry may set, in the order of TunedEntry
 OPTION_KEYS = ("variant", "tile_n", "split_k", "schedule", "copy_kblocks", "cluster_split", "raster_group",
-               "swap_ab", "multicast")
+               "swap_ab", "multicast", "skinny")
 CONFIG_KEYS = ("variant", "tile_n", "split_k", "schedule", "copy_kblocks", "cluster_split", "raster_group",
-               "swap_ab", "multicast", "grid", "stages")
+               "swap_ab", "multicast", "grid", "stages", "skinny")
 MIN_GAIN = 1.015  # tuned time at least 1.5 % below the rules' time
 ROUNDS = 3
 
 
 def options_of(cfg: dict) -> dict:
     """Plan options that reproduce a launch configuration exactly."""
+    if cfg.get("skinny"):
+        return {k: 0 for k in OPTION_KEYS if k != "skinny"} | {"skinny": 2}
     return {
         "variant": int(cfg["variant"]),
         "tile_n": int(cfg["tile_n"]),
@@ -55,6 +57,7 @@ def options_of(cfg: dict) -> dict:
         "raster_group": int(cfg["raster_group"]),
         "swap_ab": 2 if cfg["swap_ab"] else 1,
         "multicast": 2 if cfg["multicast"] == 2 else 1,
+        "skinny": 1,
     }
 
 
@@ -81,7 +84,7 @@ def header_text(rows, min_gain: float = MIN_GAIN) -> str:
         "    int64_t M, N, K;",
         "    // the options the entry sets (0 = automatic, as in bwgemm_plan_options_t)",
         "    int32_t variant, tile_n, split_k, schedule, copy_kblocks, cluster_split, raster_group, swap_ab,",
-        "        multicast;",
+        "        multicast, skinny;",
         "};",
         "",
         "// the last entry (M = 0) ends the table",
@@ -92,7 +95,7 @@ def header_text(rows, min_gain: float = MIN_GAIN) -> str:
         vals = ", ".join(str(int(o[k])) for k in OPTION_KEYS)
         lines.append(f"    {{{r['M']}, {r['N']}, {r['K']}, {vals}}},  // {r['shape']}: "
                      f"{r['rules_us']:.2f} -> {r['tuned_us']:.2f} us")
-    lines += ["    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},", "};", "", "}  // namespace bwgemm", ""]
+    lines += ["    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},", "};", "", "}  // namespace bwgemm", ""]
     return "\n".join(lines)
 
 

@@ -109,8 +109,9 @@ typedef struct {
                                  once and multicast to both pairs (CTA-pair variant,
                                  operands not swapped)                                   */
     int32_t copy_kblocks;     /* K blocks per TMA operand copy: 0 = auto (two for
-                                 compute-bound shapes), 1 = one, 2 = two (where K holds
-                                 at least two whole 64-element chunks)                   */
+                                 compute-bound shapes, four in the whole-K kernel),
+                                 1 = one, 2 = two (where K holds at least two whole
+                                 64-element chunks; either selects the main kernel)      */
     int32_t cluster_split;    /* 0 = auto, 1 = off, 2 = required: the two K slices of a
                                  one-wave split-K tile run in one cluster and exchange
                                  partials through distributed shared memory (when a
@@ -119,6 +120,11 @@ typedef struct {
                                  shape matches one of its entries exactly and every
                                  option the entry sets is left automatic, 1 = plan
                                  from the rules alone                                   */
+    int32_t skinny;           /* 0 = auto, 1 = off, 2 = required: for at most 64 rows of A
+                                 (operands swapped) and ceil(N / 64) <= SMs, the whole-K
+                                 kernel with 64 weight rows per CTA (MMA M = 64) and no
+                                 split of K; auto takes it unless another option asks
+                                 for something only the main kernel does              */
     int32_t reserved[1];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
@@ -148,12 +154,15 @@ typedef struct {
     int32_t multicast;    /* CTA pairs per cluster sharing each A tile (1 or 2);
                              a tile then spans tile_n x multicast columns        */
     int32_t copy_kblocks; /* K blocks per TMA operand copy (1 or 2; 2 applies
-                             where K holds at least two whole 64-element chunks) */
+                             where K holds at least two whole 64-element chunks;
+                             the whole-K kernel: 4 where K holds four, else 1)   */
     int32_t prefetch_kblocks; /* L2 prefetch distance of the streamed operand (0: off) */
     int32_t prefetch_b;   /* the streamed operand: 1 = B (the kernel's), 0 = A   */
     int32_t cluster_split; /* 1: split_k = 2 slices per tile inside one cluster,
                               partials exchanged in distributed shared memory    */
     int32_t tuned;         /* 1: an entry of the tuned-options table was applied */
+    int32_t skinny;        /* 1: the whole-K kernel for a few rows of A (tile_m =
+                              64 weight rows per CTA, tile_n = the MMA's N)      */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

@@ -205,7 +205,7 @@ def test_select_swapped_operands_for_small_m():
     # M <= 64 decode: C^T = B A^T, 128 rows of B per CTA, A's rows as a 64-wide
     # MMA N; 64 tiles, two K slices each, all in one wave
     for M in (1, 16, 64):
-        c = cfg(M, 8192, 8192, sms=152, pairs=76)
+        c = cfg(M, 8192, 8192, sms=152, pairs=76, skinny=1)
         assert c["swap_ab"] == 1 and c["variant"] == 1 and (c["tile_m"], c["tile_n"]) == (128, 64)
         assert c["num_tiles"] == 64 and c["split_k"] == 2 and c["split_scatter"] == 1
         assert c["grid"] == 128
@@ -270,7 +270,7 @@ def test_select_cluster_split():
     assert c["workspace_bytes"] == 0
     c = cfg(256, 8192, 8192, sms=152, pairs=76)  # 37 tiles of 224 (38 clusters of four fit)
     assert c["tile_n"] == 224 and c["cluster_split"] == 1 and c["grid"] == 37 * 4
-    c = cfg(16, 8192, 8192, sms=152, pairs=76)  # swapped: clusters of two single CTAs
+    c = cfg(16, 8192, 8192, sms=152, pairs=76, skinny=1)  # swapped: clusters of two single CTAs
     assert c["swap_ab"] == 1 and c["cluster_split"] == 1 and c["grid"] == 64 * 2
     c = cfg(256, 8192, 8192, sms=152, pairs=76, cluster_split=1)
     assert c["cluster_split"] == 0 and c["split_scatter"] == 1 and c["workspace_bytes"] > 0
@@ -303,7 +303,7 @@ def test_select_kblocks_per_copy():
     assert cfg(4096, 4096, 4096, sms=152, pairs=76)["copy_kblocks"] == 2
     assert cfg(512, 8192, 5376, sms=152, pairs=76)["copy_kblocks"] == 2
     assert cfg(256, 28672, 8192, sms=152, pairs=76)["copy_kblocks"] == 1
-    assert cfg(32, 8192, 8192, sms=152, pairs=76)["copy_kblocks"] == 1  # swapped: N' = 32
+    assert cfg(32, 8192, 8192, sms=152, pairs=76, skinny=1)["copy_kblocks"] == 1  # swapped: N' = 32
     assert cfg(256, 28672, 8192, sms=152, pairs=76, copy_kblocks=2)["copy_kblocks"] == 2
     assert cfg(4096, 4096, 64, sms=152, pairs=76)["copy_kblocks"] == 1  # one K block
 
@@ -463,10 +463,10 @@ def test_tuned_table_entries_apply(tmp_path):
     table.write_text(
         "#pragma once\n#include <cstdint>\nnamespace bwgemm {\n"
         "struct TunedEntry { int64_t M, N, K; int32_t variant, tile_n, split_k, schedule, copy_kblocks,"
-        " cluster_split, raster_group, swap_ab, multicast; };\n"
+        " cluster_split, raster_group, swap_ab, multicast, skinny; };\n"
         "constexpr TunedEntry kTunedTable[] = {\n"
-        "  {4096, 4096, 4096, 2, 224, 0, 0, 0, 0, 4, 1, 0},\n"
-        "  {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},\n};\n}\n")
+        "  {4096, 4096, 4096, 2, 224, 0, 0, 0, 0, 4, 1, 0, 0},\n"
+        "  {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0},\n};\n}\n")
     main = tmp_path / "main.cpp"
     main.write_text(
         '#include <cstdio>\n#include "bwgemm.h"\n'
@@ -495,14 +495,14 @@ def test_tune_table_header_and_options():
     rows = [
         {"shape": "a", "M": 256, "N": 8192, "K": 8192, "gain": 1.03, "rules_us": 32.0, "tuned_us": 31.07,
          "options": {"variant": 2, "tile_n": 224, "split_k": 2, "schedule": 1, "copy_kblocks": 1,
-                     "cluster_split": 1, "raster_group": 1, "swap_ab": 1, "multicast": 1}},
+                     "cluster_split": 1, "raster_group": 1, "swap_ab": 1, "multicast": 1, "skinny": 0}},
         {"shape": "b", "M": 1, "N": 8192, "K": 8192, "gain": 1.005, "rules_us": 27.0, "tuned_us": 26.9,
          "options": {"variant": 1, "tile_n": 64, "split_k": 2, "schedule": 1, "copy_kblocks": 1,
-                     "cluster_split": 2, "raster_group": 4, "swap_ab": 2, "multicast": 1}},
+                     "cluster_split": 2, "raster_group": 4, "swap_ab": 2, "multicast": 1, "skinny": 0}},
         {"shape": "c", "M": 4096, "N": 4096, "K": 4096, "gain": 1.0, "same": True, "options": None},
     ]
     text = tune_table.header_text(rows)
-    assert "{256, 8192, 8192, 2, 224, 2, 1, 1, 1, 1, 1, 1},  // a:" in text
+    assert "{256, 8192, 8192, 2, 224, 2, 1, 1, 1, 1, 1, 1, 0},  // a:" in text
     assert "{1, 8192, 8192" not in text and "{4096" not in text  # below the gain bar / same
     assert text.rstrip().endswith("}  // namespace bwgemm")
     # the options that reproduce a configuration, checked through the host planner
@@ -521,4 +521,38 @@ def test_select_raster_group_by_operand_size():
     assert binding.select_config(148, 8192, 28672, 8192, max_pairs=74)["raster_group"] == 8
     assert binding.select_config(148, 2048, 2048, 2048, max_pairs=74)["raster_group"] == 8  # 8 row blocks
     assert binding.select_config(148, 4096, 4096, 4096, max_pairs=74, raster_group=4)["raster_group"] == 4
+
+
+def test_select_whole_k_kernel_for_a_few_rows():
+    # M <= 64 rows of A (operands swapped): 64 weight rows per CTA (MMA M = 64),
+    # the rows of A as the MMA's N rounded up to 16 / 32 / 64, whole K, one wave
+    # (more than 32 rows: CTA pairs, M = 128 across the pair, each CTA copying
+    # half of A's rows)
+    for M, bn in ((1, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64)):
+        cg = 2 if bn == 64 else 1
+        c = cfg(M, 8192, 8192, sms=152, pairs=76)
+        assert c["skinny"] == 1 and c["swap_ab"] == 1 and c["variant"] == cg
+        assert (c["tile_m"], c["tile_n"], c["split_k"]) == (64 * cg, bn, 1)
+        assert c["grid"] == 128 and c["num_tiles"] == 128 // cg and c["workspace_bytes"] == 0
+        # stages of four K blocks in about 200 KiB: 40, 48 or 48 KiB per CTA
+        assert (c["stages"], c["copy_kblocks"]) == {16: (5, 4), 32: (4, 4), 64: (4, 4)}[bn]
+    # pairs: 76 fit on 152 SMs (N = 9728), 77 do not
+    assert cfg(64, 9728, 8192, sms=152, pairs=76)["skinny"] == 1
+    assert cfg(64, 9856, 8192, sms=152, pairs=76)["skinny"] == 0
+    assert cfg(64, 9728, 8192, sms=152, pairs=70)["skinny"] == 0
+    # ragged N: the last CTA's weight rows past N are zero-filled and not stored
+    assert cfg(16, 1100, 4096, sms=152, pairs=76)["grid"] == 18
+    # fewer than four whole K chunks: one K block per stage
+    assert cfg(16, 1100, 200, sms=152, pairs=76)["copy_kblocks"] == 1
+    # more tiles than SMs, or more than 64 rows: the main kernel
+    assert cfg(16, 28672, 8192, sms=152, pairs=76)["skinny"] == 0
+    assert cfg(200, 8192, 8192, sms=152, pairs=76)["skinny"] == 0
+    # an option only the main kernel has keeps it; skinny = 2 requires the whole-K form
+    assert cfg(16, 8192, 8192, sms=152, pairs=76, split_k=2)["skinny"] == 0
+    assert cfg(16, 8192, 8192, sms=152, pairs=76, skinny=1)["skinny"] == 0
+    assert cfg(16, 8192, 8192, sms=152, pairs=76, skinny=2, split_k=2)["skinny"] == 1
+    with pytest.raises(binding.BwgemmError):
+        cfg(200, 8192, 8192, sms=152, pairs=76, skinny=2)
+    with pytest.raises(binding.BwgemmError):
+        cfg(16, 8192, 8192, skinny=3)
 

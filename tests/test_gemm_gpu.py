@@ -710,3 +710,89 @@ def test_epilogue_share_of_a_traced_launch():
     e = row["epilogue"]
     assert e["ctas"] > 0 and 0.0 < e["busy_share"] <= 1.0
     assert e["exposed_us"] is not None and 0.0 <= e["exposed_share"] <= 1.0
+
+
+# ---------------------------------------------- whole-K kernel for a few rows
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("N,K", [(1088, 1024), (1104, 1000), (2048, 64), (1024, 200), (8192, 1600), (1024, 256),
+                                 (1040, 328)])
+def test_skinny_exact(M, N, K):
+    # 64 weight rows per CTA (MMA M = 64), A's rows as the MMA's N, whole K:
+    # K of one block, whole stages of four blocks only (1024, 256), whole
+    # stages then single blocks (1000, 1600, 328: 5 whole chunks and a ragged
+    # one), fewer than four chunks (200), a ragged last CTA (N not a multiple
+    # of 64)
+    A = make_matrix(M, K, "int2", seed=4000 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=4100 + N + K, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["skinny"] == 1 and c["split_k"] == 1 and c["tile_m"] == (128 if M > 32 else 64)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_skinny_normal_inputs(dtype, M):
+    A = make_matrix(M, 4096, "normal", dtype, seed=4200 + M, device="cuda")
+    B = make_matrix(8192, 4096, "weight", dtype, seed=4201, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, dtype)
+        assert p.last_config()["skinny"] == 1
+
+
+@pytest.mark.parametrize("M", [20, 50])
+@pytest.mark.parametrize("N", [1100, 1297, 1096])
+def test_skinny_strided_operands_and_columns_untouched(M, N):
+    # the row end of C inside the last output block (16 columns for one CTA,
+    # 32 for a pair), off a 16-byte boundary (1100, 1297) or on one (1096);
+    # the columns after N belong to the caller
+    K = 520
+    A = make_matrix(M, K, "int2", seed=4300, device="cuda", ld=K + 24)
+    B = make_matrix(N, K, "int2", seed=4301, device="cuda", ld=K + 8)
+    Cbuf = torch.full((M, 1320), 7.0, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0) as p:
+        run_full(p, A, B, "bf16", exact=True, out=Cbuf[:, :N])
+        assert p.last_config()["skinny"] == 1
+    assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
+
+
+def test_skinny_back_to_back_and_graph():
+    # programmatic dependent launch chains and a captured graph: each launch
+    # sees the previous one's output through C
+    A = make_matrix(16, 2048, "int2", seed=4400, device="cuda")
+    B = make_matrix(4096, 2048, "int2", seed=4401, device="cuda")
+    want = oracle.gemm(bits_of(A), bits_of(B), "bf16")
+    with binding.Plan(0) as p:
+        outs = [p.gemm(A, B) for _ in range(4)]
+        assert p.status() == 0 and p.last_config()["skinny"] == 1
+        for C in outs:
+            compare(bits_of(C), want, "bf16", 2048, exact=True)
+        C = torch.empty(16, 4096, dtype=torch.bfloat16, device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            p.gemm(A, B, out=C)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        C.zero_()
+        with torch.cuda.graph(g):
+            p.gemm(A, B, out=C)
+        g.replay()
+        torch.cuda.synchronize()
+        assert p.status() == 0
+        compare(bits_of(C), want, "bf16", 2048, exact=True)
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_skinny_bounded_wait_reports_timeout(M):
+    # one CTA (16 rows) and a CTA pair (64 rows): the even CTA's producer
+    # never fills a stage, every wait of both CTAs ends
+    A = make_matrix(M, 4096, "int2", seed=4500, device="cuda")
+    B = make_matrix(2048, 4096, "int2", seed=4501, device="cuda")
+    with binding.Plan(0, stall_kblock=3, timeout_ns=20_000_000) as p:
+        p.gemm(A, B)
+        assert p.last_config()["skinny"] == 1
+        assert p.status() == 6  # BWGEMM_ERR_TIMEOUT, no trap
+        assert p.last_device_status() != 0
+    with binding.Plan(0) as p:  # the context is still usable
+        run_full(p, A, B, "bf16", exact=True)

@@ -232,6 +232,42 @@ def time_each(fn, sets, iters, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def time_graph(fn, sets, launches, per_graph=20):
+    """Milliseconds per launch with the host out of the loop: `per_graph`
+    launches (rotating input sets) captured once in a CUDA graph on the
+    current stream, the graph replayed back to back between two events.  For
+    launches of a few tens of microseconds the host's cost per call (Python,
+    argument checks, the driver) is close to the GPU's time, so back-to-back
+    eager launches can measure the host; both arms are timed this way too."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(3):
+            fn(*sets[i % len(sets)])
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(per_graph):
+            fn(*sets[i % len(sets)])
+    replays = max(3, launches // per_graph)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(replays):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (replays * per_graph)
+    del g
+    return ms
+
+
 def aggregate(seconds: float, work_per_step: float, steps: int):
     """Throughput of one GPU's timed region.  Returns (seconds, work_per_second)."""
     return seconds, work_per_step * steps / seconds
@@ -239,11 +275,14 @@ def aggregate(seconds: float, work_per_step: float, steps: int):
 
 def compact_shape(rec: dict) -> dict:
     """The short form of one shape's record that ends the JSON line: time per
-    launch, fraction of its roofline (bound), cuBLAS's time on the same
-    tensors and the median SM clock while it ran."""
+    launch (us), fraction of its roofline keyed by the bound ("hbm" or
+    "tensor"), cuBLAS's time on the same tensors (cb_us), both again under
+    CUDA graph replay (g_us, cb_g_us) and the median SM clock while it ran."""
     r = rec["roofline"]
-    out = {"us": rec["us"], "frac": r["frac"], "bound": r["bound"],
-           "cublas_us": rec.get("cublas_us")}
+    out = {"us": rec["us"], r["bound"]: r["frac"], "cb_us": rec.get("cublas_us")}
+    if rec.get("graph_us") is not None:
+        out["g_us"] = rec["graph_us"]
+        out["cb_g_us"] = rec.get("cublas_graph_us")
     mhz = (rec.get("clocks") or {}).get("sm_mhz")
     if mhz is not None:
         out["mhz"] = int(mhz)
@@ -473,7 +512,13 @@ def run_ours(args):
                 raise SystemExit(f"device status error on {name}")
             cfg = plan.last_config()
             med = statistics.median(time_each(ours, ssets, 50, stream)) / 1e3
+            # both arms also with the host out of the loop (CUDA graph replay,
+            # launches on the capturing stream), median of three timings
+            n_g = int(min(2000, max(60, 0.05 / max(t, 1e-7))))
+            g_ours = statistics.median(
+                time_graph(lambda A, B, C: plan.gemm(A, B, out=C), ssets, n_g) for _ in range(3)) / 1e3
             t_cb, _ = steady(cublas, ssets)
+            g_cb = statistics.median(time_graph(cublas, ssets, n_g) for _ in range(3)) / 1e3
             r = roofline_entry(s, t, peaks)
             shapes[name] = {"M": s.M, "N": s.N, "K": s.K, "dtype": s.dtype,
                             "us": round(t * 1e6, 2), "median_us": round(med * 1e6, 2),
@@ -482,6 +527,8 @@ def run_ours(args):
                             "roofline": r,
                             "cublas_us": round(t_cb * 1e6, 2),
                             "cublas_tflops": round(s.flops / t_cb / 1e12, 1),
+                            "graph_us": round(g_ours * 1e6, 2),
+                            "cublas_graph_us": round(g_cb * 1e6, 2),
                             "kernel_config": {k: cfg[k] for k in ("variant", "tile_m", "tile_n",
                                                                   "split_k", "schedule", "grid")}}
             del ssets

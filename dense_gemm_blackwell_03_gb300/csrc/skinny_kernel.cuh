@@ -21,7 +21,8 @@
 // 128 contiguous bytes of each row) where K allows, one K block at a time for
 // what is left: a stage of four K blocks of 64 weight rows is one 32 KiB
 // copy, which shared memory fills at about 1.6 times the rate it fills from
-// 16 KiB copies.
+// 16 KiB copies.  A pair takes three K blocks per stage, so that six stages
+// fit and more weight bytes are in flight.
 //
 //   warp 0      TMA producer (the whole warp walks the stages; an elected lane
 //               issues); full/empty mbarrier pairs per stage.  In a pair both

@@ -534,16 +534,19 @@ def test_select_whole_k_kernel_for_a_few_rows():
         assert c["skinny"] == 1 and c["swap_ab"] == 1 and c["variant"] == cg
         assert (c["tile_m"], c["tile_n"], c["split_k"]) == (64 * cg, bn, 1)
         assert c["grid"] == 128 and c["num_tiles"] == 128 // cg and c["workspace_bytes"] == 0
-        # stages of four K blocks in about 200 KiB: 40, 48 or 48 KiB per CTA
-        assert (c["stages"], c["copy_kblocks"]) == {16: (5, 4), 32: (4, 4), 64: (4, 4)}[bn]
+        # stages of four K blocks (three for a pair) in about 216 KiB: 40, 48
+        # or 36 KiB per CTA
+        assert (c["stages"], c["copy_kblocks"]) == {16: (5, 4), 32: (4, 4), 64: (6, 3)}[bn]
     # pairs: 76 fit on 152 SMs (N = 9728), 77 do not
     assert cfg(64, 9728, 8192, sms=152, pairs=76)["skinny"] == 1
     assert cfg(64, 9856, 8192, sms=152, pairs=76)["skinny"] == 0
     assert cfg(64, 9728, 8192, sms=152, pairs=70)["skinny"] == 0
     # ragged N: the last CTA's weight rows past N are zero-filled and not stored
     assert cfg(16, 1100, 4096, sms=152, pairs=76)["grid"] == 18
-    # fewer than four whole K chunks: one K block per stage
+    # fewer whole K chunks than a stage holds: one K block per stage
     assert cfg(16, 1100, 200, sms=152, pairs=76)["copy_kblocks"] == 1
+    assert cfg(64, 1100, 200, sms=152, pairs=76)["copy_kblocks"] == 3
+    assert cfg(64, 1100, 128, sms=152, pairs=76)["copy_kblocks"] == 1
     # more tiles than SMs, or more than 64 rows: the main kernel
     assert cfg(16, 28672, 8192, sms=152, pairs=76)["skinny"] == 0
     assert cfg(200, 8192, 8192, sms=152, pairs=76)["skinny"] == 0

@@ -29,14 +29,17 @@ def test_compact_shape_summary():
     sys.path.insert(0, ROOT)
     import bench
     rec = {"us": 31.5, "roofline": {"frac": 0.6561, "bound": "hbm"}, "cublas_us": 29.4,
-           "clocks": {"sm_mhz": 2017.0}, "median_us": 37.0, "kernel_config": {"grid": 128}}
-    assert bench.compact_shape(rec) == {"us": 31.5, "frac": 0.6561, "bound": "hbm",
-                                        "cublas_us": 29.4, "mhz": 2017}
+           "clocks": {"sm_mhz": 2017.0}, "median_us": 37.0, "kernel_config": {"grid": 128},
+           "graph_us": 2347.16, "cublas_graph_us": 2287.07}
+    assert bench.compact_shape(rec) == {"us": 31.5, "hbm": 0.6561, "cb_us": 29.4,
+                                        "g_us": 2347.16, "cb_g_us": 2287.07, "mhz": 2017}
+    # the longest values: a tensor-bound shape of a few milliseconds
+    rec = dict(rec, us=2347.16, cublas_us=2287.07, roofline={"frac": 0.8599, "bound": "tensor"})
     # the twelve shapes besides the headline stay short enough for a
     # 1500-character tail of the output (the line is printed without spaces)
     line = json.dumps({name: bench.compact_shape(rec) for name in bench.EXTRA_SHAPES},
                       separators=(",", ":"))
-    assert len(line) < 1200
+    assert len(line) < 1300
 
 
 def test_reference_arm_json_line():

@@ -100,3 +100,11 @@ def test_clock_sampler_uses_samples_inside_the_timed_region():
     s.proc = _FakeSmi("\n".join(lines))
     c = s.stop()
     assert c["samples_under_load"] == 0 and c["selection"].startswith("all samples")
+
+
+def test_tensor_peak_regime_follows_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.tensor_peak_regime(0.004) == "burst"
+    assert bench.tensor_peak_regime(1.07) == "sustained"
+    assert bench.tensor_peak_regime(bench.SUSTAINED_REGION_S) == "sustained"

@@ -53,7 +53,8 @@ EXTRA_SHAPES = ["square4096_fp16", "prefill_attn_out", "prefill_mlp_up", "decode
 PAGES_4096_BF16 = 1772.9  # TFLOP/s, the Blackwell deep dive's final kernel, on B200
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "gemm_sm103.cu", "planner.cpp",
-                  "api.cpp", "internal.h", "skinny_kernel.cuh", "skinny_sm103.cu"]
+                  "api.cpp", "internal.h", "skinny_kernel.cuh", "skinny_sm103.cu", "wholek_kernel.cuh",
+                  "wholek_sm103.cu"]
 
 
 def log(*a):

@@ -83,6 +83,7 @@ class PlanOptions(ctypes.Structure):
         ("cluster_split", ctypes.c_int32),
         ("tuned_table", ctypes.c_int32),
         ("skinny", ctypes.c_int32),
+        ("wholek", ctypes.c_int32),
         ("reserved", ctypes.c_int32 * 1),
     ]
 
@@ -113,6 +114,7 @@ class Config(ctypes.Structure):
         ("cluster_split", ctypes.c_int32),
         ("tuned", ctypes.c_int32),
         ("skinny", ctypes.c_int32),
+        ("wholek", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -20,9 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbwgemm.so")
 
-SOURCES = ["gemm_sm103.cu", "skinny_sm103.cu", "api.cpp", "planner.cpp", "noalloc.cu", "probe.cu",
+SOURCES = ["gemm_sm103.cu", "skinny_sm103.cu", "wholek_sm103.cu", "api.cpp", "planner.cpp", "noalloc.cu", "probe.cu",
            "microbench.cu"]
-HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "skinny_kernel.cuh", "kernel_params.h", "internal.h", "tuned_table.h"]
+HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "skinny_kernel.cuh", "wholek_kernel.cuh", "kernel_params.h", "internal.h", "tuned_table.h"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

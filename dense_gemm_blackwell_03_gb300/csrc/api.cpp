@@ -304,6 +304,52 @@ bwgemm_status_t enqueue_skinny(bwgemm_plan_t plan, const bwgemm_plan_options_t& 
     return BWGEMM_OK;
 }
 
+// The whole-K pair kernel for 129 to 256 rows of A: A in boxes of 128 rows
+// (each CTA of a pair its half, zero-filled past M), B in boxes of
+// wholek_bn / 2 weight rows, 3-D views of wholek_kblocks() K chunks, C in
+// boxes of 32 rows x wholek_bn columns (clipped at M and N).
+bwgemm_status_t enqueue_wholek(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, const Selection& sel,
+                               const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, cudaStream_t stream)
+{
+    bwgemm_status_t st;
+    const uint32_t bn = uint32_t(sel.wholek_bn);
+    if ((st = get_tmap(plan->tmaps[0], A, dtype, K, M, lda, kTileK, 128u, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            BWGEMM_OK ||
+        (st = get_tmap(plan->tmaps[1], B, dtype, K, N, ldb, kTileK, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            BWGEMM_OK ||
+        (st = get_tmap(plan->tmaps[2], C, dtype, N, M, ldc, bn, 32u, CU_TENSOR_MAP_SWIZZLE_NONE)) != BWGEMM_OK)
+        return st;
+    GemmParams p = make_params(sel, M, N, K, dtype);
+    const int64_t chunks = K / kTileK;
+    const int kps = wholek_kblocks(int(bn));
+    const bool views = kps > 1 && chunks >= kps;
+    if (views && ((st = get_tmap3(plan->tmaps[3], A, dtype, chunks, M, lda, 128u, uint32_t(kps))) != BWGEMM_OK ||
+                  (st = get_tmap3(plan->tmaps[4], B, dtype, chunks, N, ldb, bn / 2, uint32_t(kps))) != BWGEMM_OK))
+        return st;
+    p.k_chunks_a = views ? int32_t(chunks) : 0;
+    p.k_chunks_b = views ? int32_t(chunks) : 0;
+    p.timeout_ns = opts.timeout_ns ? opts.timeout_ns : 4000000000ull;
+    p.status = plan->d_status;
+    p.c = static_cast<uint16_t*>(C);
+    p.ldc = ldc;
+    p.stall_kblock = opts.stall_kblock;
+    if (plan->d_trace) {
+        if (sel.cfg.grid > plan->trace_ctas)
+            return BWGEMM_ERR_UNSUPPORTED;
+        p.trace = plan->d_trace;
+    }
+    const CUtensorMap& a3 = views ? plan->tmaps[3].map : plan->tmaps[0].map;
+    const CUtensorMap& b3 = views ? plan->tmaps[4].map : plan->tmaps[1].map;
+    if (launch_wholek(int(bn), plan->tmaps[0].map, plan->tmaps[1].map, a3, b3, plan->tmaps[2].map, p,
+                      sel.cfg.grid, stream, opts.pdl_off == 0) != cudaSuccess)
+        return BWGEMM_ERR_CUDA;
+    plan->last = sel.cfg;
+    plan->last_grid = sel.cfg.grid;
+    plan->launches += 1;
+    return BWGEMM_OK;
+}
+
 bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, const void* A,
                         const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                         int64_t ldb, int64_t ldc, bwgemm_dtype_t dtype, cudaStream_t stream)
@@ -330,6 +376,8 @@ bwgemm_status_t enqueue(bwgemm_plan_t plan, const bwgemm_plan_options_t& opts, c
         return st;
     if (sel.skinny_bn > 0)
         return enqueue_skinny(plan, opts, sel, A, B, C, M, N, K, lda, ldb, ldc, dtype, stream);
+    if (sel.wholek_bn > 0)
+        return enqueue_wholek(plan, opts, sel, A, B, C, M, N, K, lda, ldb, ldc, dtype, stream);
     const Variant& v = kVariants[sel.variant_idx];
     const uint32_t b_rows = uint32_t(v.cg == 1 ? v.bn : v.bn / 2);
     // the MMA's A operand (128-row side) and B operand; exchanged when swapped

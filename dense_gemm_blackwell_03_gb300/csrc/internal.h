@@ -99,6 +99,18 @@ cudaError_t launch_skinny(int bn, const CUtensorMap& w, const CUtensorMap& x, co
                           const CUtensorMap& x3, const CUtensorMap& c, const GemmParams& p, int grid,
                           cudaStream_t stream, bool pdl);
 
+// The whole-K pair kernel for 129 to 256 rows of A (wholek_kernel.cuh): all
+// rows of A on the MMA's M side (256 over a CTA pair), bn weight rows per
+// pair (the MMA's N, a multiple of 16), no split of K.  Stages of
+// wholek_kblocks() K blocks in about 224 KiB; the output staging reuses the
+// ring.  The widths the library is built for, narrowest first:
+constexpr int kWholeKWidths[] = {96, 112, 128, 144, 160, 192};
+constexpr int wholek_kblocks(int /*bn*/) { return 2; }
+constexpr int wholek_stages(int bn) { return (224 * 1024) / (wholek_kblocks(bn) * (128 + bn / 2) * 128); }
+cudaError_t launch_wholek(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a3,
+                          const CUtensorMap& b3, const CUtensorMap& c, const GemmParams& p, int grid,
+                          cudaStream_t stream, bool pdl);
+
 // Sizes of the split-K workspace regions.
 constexpr uint64_t kCounterRegionBytes = 1ull << 20;  // per-(tile, cta, warp) arrival counters
 
@@ -106,6 +118,7 @@ struct Selection {
     bwgemm_config_t cfg;
     int variant_idx;  // into kVariants; -1 for the whole-K kernel of skinny_bn > 0
     int skinny_bn;    // > 0: the whole-K kernel for a few rows of A, MMA N = skinny_bn
+    int wholek_bn;    // > 0: the whole-K pair kernel, wholek_bn weight rows per pair
     bool swap;  // the kernel sees the problem N x M (A and B exchanged)
     int num_m_blocks, num_n_blocks, num_k_blocks;
     int64_t sk_iters;

@@ -96,6 +96,7 @@ bwgemm_status_t noalloc_select(int num_sms, int max_pairs, int64_t M, int64_t N,
     opts.multicast = 1;      // one CTA pair per cluster: the scratch below is sized for it
     opts.cluster_split = 1;  // slices reduce through the scratch array, not in a cluster
     opts.skinny = 1;         // the split-K kernel, also for a few rows of A
+    opts.wholek = 1;         // and for up to 256 rows
     // plan as if the workspace were unbounded, then hold the need against the array
     const bwgemm_status_t st = select_config(num_sms, max_pairs, 0, M, N, K, opts, ~uint64_t(0), sel);
     if (st != BWGEMM_OK)

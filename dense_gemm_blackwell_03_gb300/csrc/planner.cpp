@@ -196,6 +196,64 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
         }
     }
 
+    // 129 to 256 rows of A, operands in order: the whole-K pair kernel with all
+    // rows of A on the MMA's M side (256 over the pair) and the narrowest block
+    // of weight rows whose blocks fit the co-resident pairs once (N = 10240:
+    // 72 blocks of 144), so that no K split and no exchange of partials is
+    // needed.  Automatic only where the main kernel would take a pair tile
+    // wider than 256 columns (two MMAs per K step into a single-buffered
+    // accumulator, split in clusters): there it measured ~2 % faster (decode
+    // QKV), while against 256-wide tiles split in clusters it was 2-10 %
+    // slower (N = 8192, K = 8192 and 28672).  wholek = 2 requires it.
+    if (opts.wholek < 0 || opts.wholek > 2)
+        return BWGEMM_ERR_INVALID_ARG;
+    int wbn = 0;
+    for (int w : kWholeKWidths)
+        if (wbn == 0 && ceil_div(N, int64_t(w)) <= max_pairs && 2 * ceil_div(N, int64_t(w)) <= num_sms)
+            wbn = w;
+    const int64_t wk_units = wbn ? ceil_div(N, int64_t(wbn)) : 0;  // pairs
+    const bool wk_fits = !swap && M > 128 && M <= 256 && wbn > 0 &&
+                         (opts.max_ctas == 0 || 2 * wk_units <= opts.max_ctas);
+    const bool wk_forced_other = opts.variant != BWGEMM_VARIANT_AUTO || opts.tile_n != 0 || opts.split_k > 1 ||
+                                 clc || opts.schedule == BWGEMM_SCHEDULE_STREAM_K || mc != 1 ||
+                                 opts.cluster_split == 2 || opts.prefetch > 0 || opts.copy_kblocks != 0 ||
+                                 opts.raster_group > 0 || opts.swap_ab == 2;
+    if (opts.wholek == 2 && !wk_fits)
+        return BWGEMM_ERR_UNSUPPORTED;
+    auto wholek_selection = [&]() {
+        Selection sel;
+        std::memset(&sel, 0, sizeof(sel));
+        sel.variant_idx = -1;
+        sel.wholek_bn = wbn;
+        sel.swap = false;
+        sel.num_m_blocks = 1;
+        sel.num_n_blocks = int(wk_units);
+        sel.num_k_blocks = int(num_kb);
+        sel.cfg.variant = BWGEMM_VARIANT_2SM;
+        sel.cfg.tile_m = 256;
+        sel.cfg.tile_n = wbn;
+        sel.cfg.tile_k = kTileK;
+        sel.cfg.stages = wholek_stages(wbn);
+        sel.cfg.split_k = 1;
+        sel.cfg.raster_group = 1;
+        sel.cfg.num_tiles = int32_t(wk_units);
+        sel.cfg.num_units = int32_t(wk_units);
+        sel.cfg.grid = int32_t(2 * wk_units);
+        sel.cfg.schedule = BWGEMM_SCHEDULE_TILES;
+        sel.cfg.dp_tiles = int32_t(wk_units);
+        sel.cfg.workers = int32_t(wk_units);
+        sel.cfg.swap_ab = 0;
+        sel.cfg.multicast = 1;
+        sel.cfg.copy_kblocks = K / kTileK >= wholek_kblocks(wbn) ? wholek_kblocks(wbn) : 1;
+        sel.cfg.tuned = tuned ? 1 : 0;
+        sel.cfg.wholek = 1;
+        return sel;
+    };
+    if (wk_fits && opts.wholek == 2) {
+        *out = wholek_selection();
+        return BWGEMM_OK;
+    }
+
     // Tile width of the pair form: 224, 320 or 384 instead of 256 columns
     // when the problem then fits one wave clearly better.  N = 8192 makes 32
     // tiles of 256 (x 2 K slices, or x 2 row blocks: 64 of 76 pairs) but 37
@@ -416,6 +474,10 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     sel.cfg.prefetch_kblocks = opts.prefetch > 0 ? opts.prefetch : 0;
     sel.cfg.prefetch_b = (Nk >= Mk) ? 1 : 0;
 
+    if (wk_fits && opts.wholek == 0 && !wk_forced_other && sel.cfg.tile_n > 256) {
+        *out = wholek_selection();
+        return BWGEMM_OK;
+    }
     *out = sel;
     return BWGEMM_OK;
 }
@@ -434,6 +496,25 @@ GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bw
 {
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
+    if (sel.wholek_bn > 0) {
+        // the whole-K pair kernel: the caller's problem, all of M in one pair
+        p.M = int32_t(M);
+        p.N = int32_t(N);
+        p.K = int32_t(K);
+        p.num_m_blocks = 1;
+        p.num_n_blocks = sel.num_n_blocks;
+        p.num_k_blocks = sel.num_k_blocks;
+        p.num_tiles = sel.cfg.num_tiles;
+        p.split_k = 1;
+        p.dp_tiles = sel.cfg.num_tiles;
+        p.dp_units = sel.cfg.num_tiles;
+        p.raster_group = 1;
+        p.dtype = int32_t(dtype);
+        p.idesc = make_idesc(int(dtype), 256, sel.wholek_bn);
+        p.stall_kblock = -1;
+        p.ks = 1;
+        return p;
+    }
     if (sel.skinny_bn > 0) {
         // the whole-K kernel: the weight rows (the caller's N) are its M
         p.M = int32_t(N);

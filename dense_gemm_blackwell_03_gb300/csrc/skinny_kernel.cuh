@@ -43,10 +43,11 @@
 //               clipped; a block holding a row end off a 16-byte boundary is
 //               written with plain stores).
 //
-// Before its dependency wait the producer prefetches the CTA's first
-// kSkPrefetchKBlocks K blocks of weights into L2: the previous kernel on the
-// stream is still finishing, HBM would otherwise idle, and a prefetch only
-// warms L2, so it is safe even if that kernel writes the weights.
+// At entry, before the set-up and the dependency wait, the producer lane
+// prefetches the CTA's first kSkPrefetchKBlocks K blocks of weights into L2:
+// the previous kernel on the stream is still finishing, HBM would otherwise
+// idle, and a prefetch only warms L2, so it is safe even if that kernel
+// writes the weights.
 //
 // Every wait is bounded (the main kernel's wait_phase); after an abort the
 // kernel drains its MMAs and loads before it releases TMEM and shared memory,
@@ -156,6 +157,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             ptx::prefetch_tensormap(&tmap_w3);
         if (p.k_chunks_b >= KPS)
             ptx::prefetch_tensormap(&tmap_x3);
+        // the first weight blocks into L2 at once, ahead of the set-up and of
+        // the dependency wait
+        if (p.k_chunks_a >= KPS) {
+#pragma unroll 1
+            for (int kb = 0; kb + KPS <= p.k_chunks_a && kb < kSkPrefetchKBlocks; kb += KPS)
+                ptx::tma_prefetch_3d(&tmap_w3, 0, n0, kb);
+        }
     }
     if (warp == 2 && lane == 0)
         ptx::prefetch_tensormap(&tmap_c);
@@ -179,11 +187,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && p.k_chunks_a >= KPS) {
-#pragma unroll 1
-            for (int kb = 0; kb + KPS <= p.k_chunks_a && kb < kSkPrefetchKBlocks; kb += KPS)
-                ptx::tma_prefetch_3d(&tmap_w3, 0, n0, kb);
-        }
         ptx::grid_dependency_wait();
         if (lane == 0)
             trace_mark(p, kTraceReady);

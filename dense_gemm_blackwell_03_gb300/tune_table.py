@@ -38,7 +38,7 @@ SWEEP_SHAPES = ["square4096", "prefill_attn_out", "prefill_mlp_up", "decode_attn
 OPTION_KEYS = ("variant", "tile_n", "split_k", "schedule", "copy_kblocks", "cluster_split", "raster_group",
                "swap_ab", "multicast", "skinny")
 CONFIG_KEYS = ("variant", "tile_n", "split_k", "schedule", "copy_kblocks", "cluster_split", "raster_group",
-               "swap_ab", "multicast", "grid", "stages", "skinny")
+               "swap_ab", "multicast", "grid", "stages", "skinny", "wholek")
 MIN_GAIN = 1.015  # tuned time at least 1.5 % below the rules' time
 ROUNDS = 3
 
@@ -47,6 +47,8 @@ def options_of(cfg: dict) -> dict:
     """Plan options that reproduce a launch configuration exactly."""
     if cfg.get("skinny"):
         return {k: 0 for k in OPTION_KEYS if k != "skinny"} | {"skinny": 2}
+    if cfg.get("wholek"):  # the whole-K pair kernel: its own planner rule, no table entry
+        return {k: 0 for k in OPTION_KEYS}
     return {
         "variant": int(cfg["variant"]),
         "tile_n": int(cfg["tile_n"]),

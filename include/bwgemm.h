@@ -125,6 +125,14 @@ typedef struct {
                                  kernel with 64 weight rows per CTA (MMA M = 64) and no
                                  split of K; auto takes it unless another option asks
                                  for something only the main kernel does              */
+    int32_t wholek;           /* 0 = auto, 1 = off, 2 = required: for 129 to 256 rows of
+                                 A (operands not swapped), the whole-K kernel on CTA
+                                 pairs with all rows of A on the MMA's M side (256 over
+                                 the pair) and a block of weight rows (96-192) sized so
+                                 that the blocks fill the pairs once, no split of K;
+                                 auto takes it where the main kernel would use a pair
+                                 tile wider than 256 columns and no other option asks
+                                 for the main kernel                                  */
     int32_t reserved[1];      /* must be zero                                            */
 } bwgemm_plan_options_t;
 
@@ -163,6 +171,8 @@ typedef struct {
     int32_t tuned;         /* 1: an entry of the tuned-options table was applied */
     int32_t skinny;        /* 1: the whole-K kernel for a few rows of A (tile_m =
                               64 weight rows per CTA, tile_n = the MMA's N)      */
+    int32_t wholek;        /* 1: the whole-K pair kernel for 129-256 rows of A
+                              (tile_m = 256, tile_n = weight rows per pair)      */
 } bwgemm_config_t;
 
 /* Fill *opts with the defaults (all automatic, stall_kblock = -1). */

@@ -159,10 +159,13 @@ def test_select_decode_shapes():
         assert c["tile_n"] == 224 and c["num_tiles"] == 37 and c["cluster_split"] == 1
         assert c["grid"] == 148
     # fused QKV: 40 tiles of 256 -- 2 slices would not fit one wave (stream-K);
-    # 32 tiles of 320 (two MMAs per K step) x 2 slices in 32 clusters of four
-    c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1)
+    # 32 tiles of 320 (two MMAs per K step) x 2 slices in 32 clusters of four,
+    # where the whole-K pair kernel (72 blocks of 144 weight rows) is taken
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1, wholek=1)
     assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
     assert c["cluster_split"] == 1 and c["grid"] == 128 and c["stages"] == 6
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1)
+    assert c["wholek"] == 1 and c["tile_n"] == 144 and c["num_tiles"] == 72 and c["grid"] == 144
     c = cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, swap_ab=1, tile_n=256)
     assert c["schedule"] == binding.SCHEDULE_STREAM_K and c["workers"] == 76 and c["grid"] == 152
     # MLP up: 112 tiles of 256 = 1.47 waves (stream-K); 75 tiles of 384 (two
@@ -279,8 +282,8 @@ def test_select_cluster_split():
     assert c["cluster_split"] == 0
     with pytest.raises(binding.BwgemmError):
         cfg(256, 10240, 8192, sms=152, pairs=76, cluster_split=2, tile_n=256)
-    # 32 tiles of 320 fit
-    c = cfg(256, 10240, 8192, sms=152, pairs=76)
+    # 32 tiles of 320 fit (the whole-K pair kernel, taken there by default, off)
+    c = cfg(256, 10240, 8192, sms=152, pairs=76, wholek=1)
     assert c["tile_n"] == 320 and c["cluster_split"] == 1
     with pytest.raises(binding.BwgemmError):
         cfg(256, 8192, 8192, cluster_split=3)
@@ -559,3 +562,32 @@ def test_select_whole_k_kernel_for_a_few_rows():
     with pytest.raises(binding.BwgemmError):
         cfg(16, 8192, 8192, skinny=3)
 
+
+
+def test_select_whole_k_pair_kernel():
+    # 129..256 rows of A, operands in order: all rows on the MMA's M side (256
+    # over a pair), the narrowest block of weight rows (96, 112, ... 192) whose
+    # blocks fit the 76 pairs once; stages of two K blocks in about 224 KiB
+    for M in (129, 200, 256):
+        c = cfg(M, 8192, 8192, sms=152, pairs=76, wholek=2)
+        assert c["wholek"] == 1 and c["variant"] == 2 and (c["tile_m"], c["tile_n"]) == (256, 112)
+        assert c["num_tiles"] == 74 and c["grid"] == 148 and c["split_k"] == 1
+        assert c["stages"] == 4 and c["copy_kblocks"] == 2 and c["workspace_bytes"] == 0
+    assert cfg(256, 6144, 4096, sms=152, pairs=76, wholek=2)["tile_n"] == 96   # 64 blocks
+    assert cfg(256, 12288, 4096, sms=152, pairs=76, wholek=2)["tile_n"] == 192  # 64 blocks
+    with pytest.raises(binding.BwgemmError):  # 74 pairs do not fit 140 CTAs
+        cfg(256, 8192, 4096, sms=152, pairs=76, wholek=2, max_ctas=140)
+    assert cfg(256, 8192, 100, sms=152, pairs=76, wholek=2)["copy_kblocks"] == 1  # one whole chunk
+    # automatic only where the main kernel would take a tile wider than 256
+    assert cfg(256, 8192, 8192, sms=152, pairs=76, quads=36)["wholek"] == 0
+    assert cfg(200, 10240, 8192, sms=152, pairs=76, quads=36)["wholek"] == 1
+    assert cfg(256, 12288, 8192, sms=152, pairs=76, quads=36)["wholek"] == 0  # 256-wide main tiles
+    # an option only the main kernel has keeps it; wholek = 1 turns it off
+    assert cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, tile_n=320)["wholek"] == 0
+    assert cfg(256, 10240, 8192, sms=152, pairs=76, quads=36, wholek=1)["wholek"] == 0
+    # outside its range wholek = 2 is refused
+    for M, N in ((128, 8192), (257, 8192), (256, 28672)):
+        with pytest.raises(binding.BwgemmError):
+            cfg(M, N, 8192, sms=152, pairs=76, wholek=2)
+    with pytest.raises(binding.BwgemmError):
+        cfg(256, 8192, 8192, sms=152, pairs=76, wholek=3)

@@ -305,15 +305,20 @@ def test_wide_tiles_exact(M, N, K, opts, tile_n):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_tile320_auto_qkv_family(dtype):
-    # the planner's choice for one row block over N = 10240 (32 tiles of 320,
-    # two K slices each in one cluster) on N(0,1) activations and N(0, 0.02^2)
-    # weights
+    # the main kernel's choice for one row block over N = 10240 (32 tiles of
+    # 320, two K slices each in one cluster; the planner's default there is the
+    # whole-K pair kernel, turned off here) on N(0,1) activations and
+    # N(0, 0.02^2) weights
     A = make_matrix(256, 1024, "normal", dtype, seed=3730, device="cuda")
     B = make_matrix(10240, 1024, "weight", dtype, seed=3731, device="cuda")
-    with binding.Plan(0) as p:
+    with binding.Plan(0, wholek=1) as p:
         run_full(p, A, B, dtype)
         c = p.last_config()
         assert c["tile_n"] == 320 and c["num_tiles"] == 32 and c["split_k"] == 2
+    with binding.Plan(0) as p:  # the default: 72 blocks of 144 weight rows, whole K
+        run_full(p, A, B, dtype)
+        c = p.last_config()
+        assert c["wholek"] == 1 and c["tile_n"] == 144 and c["num_tiles"] == 72
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
@@ -795,4 +800,84 @@ def test_skinny_bounded_wait_reports_timeout(M):
         assert p.status() == 6  # BWGEMM_ERR_TIMEOUT, no trap
         assert p.last_device_status() != 0
     with binding.Plan(0) as p:  # the context is still usable
+        run_full(p, A, B, "bf16", exact=True)
+
+
+# ------------------------------------- whole-K pair kernel for 129-256 rows
+@pytest.mark.parametrize("M", [129, 200, 256])
+@pytest.mark.parametrize("N,K", [(8192, 1024), (1104, 1000), (2048, 64), (1040, 200), (10240, 328)])
+def test_wholek_exact(M, N, K):
+    # all rows of A on the MMA's M side (256 over a CTA pair), a block of
+    # weight rows per pair sized to fill the pairs once, whole K: K of one
+    # block, stages of two K blocks then a single one (1000: 15 whole chunks
+    # and a ragged one; 328: 5 and a ragged one), fewer chunks than a stage
+    # (200), ragged N (1104, 1040), a wide N (10240: blocks of 144)
+    A = make_matrix(M, K, "int2", seed=5000 + M, device="cuda")
+    B = make_matrix(N, K, "int2", seed=5100 + N + K, device="cuda")
+    with binding.Plan(0, wholek=2) as p:
+        run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["wholek"] == 1 and c["split_k"] == 1 and c["tile_m"] == 256 and c["variant"] == 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M", [200, 256])
+def test_wholek_normal_inputs(dtype, M):
+    A = make_matrix(M, 4096, "normal", dtype, seed=5200 + M, device="cuda")
+    B = make_matrix(8192, 4096, "weight", dtype, seed=5201, device="cuda")
+    with binding.Plan(0, wholek=2) as p:
+        run_full(p, A, B, dtype)
+        assert p.last_config()["wholek"] == 1
+
+
+@pytest.mark.parametrize("N", [1100, 1297, 1096])
+def test_wholek_strided_operands_and_columns_untouched(N):
+    # the row end of C inside the last block of weight rows, off a 16-byte
+    # boundary (1100, 1297) or on one (1096); the columns after N belong to
+    # the caller
+    M, K = 150, 520
+    A = make_matrix(M, K, "int2", seed=5300, device="cuda", ld=K + 24)
+    B = make_matrix(N, K, "int2", seed=5301, device="cuda", ld=K + 8)
+    Cbuf = torch.full((M, 1320), 7.0, dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0, wholek=2) as p:
+        run_full(p, A, B, "bf16", exact=True, out=Cbuf[:, :N])
+        assert p.last_config()["wholek"] == 1
+    assert torch.all(Cbuf[:, N:] == 7.0), "wrote outside the output view"
+
+
+def test_wholek_back_to_back_and_graph():
+    A = make_matrix(256, 2048, "int2", seed=5400, device="cuda")
+    B = make_matrix(4096, 2048, "int2", seed=5401, device="cuda")
+    want = oracle.gemm(bits_of(A), bits_of(B), "bf16")
+    with binding.Plan(0, wholek=2) as p:
+        outs = [p.gemm(A, B) for _ in range(4)]
+        assert p.status() == 0 and p.last_config()["wholek"] == 1
+        for C in outs:
+            compare(bits_of(C), want, "bf16", 2048, exact=True)
+        C = torch.empty(256, 4096, dtype=torch.bfloat16, device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            p.gemm(A, B, out=C)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        C.zero_()
+        with torch.cuda.graph(g):
+            p.gemm(A, B, out=C)
+        g.replay()
+        torch.cuda.synchronize()
+        assert p.status() == 0
+        compare(bits_of(C), want, "bf16", 2048, exact=True)
+
+
+def test_wholek_bounded_wait_reports_timeout():
+    # the even CTA's producer never fills a stage: every wait of both CTAs ends
+    A = make_matrix(256, 4096, "int2", seed=5500, device="cuda")
+    B = make_matrix(2048, 4096, "int2", seed=5501, device="cuda")
+    with binding.Plan(0, wholek=2, stall_kblock=3, timeout_ns=20_000_000) as p:
+        p.gemm(A, B)
+        assert p.last_config()["wholek"] == 1
+        assert p.status() == 6  # BWGEMM_ERR_TIMEOUT, no trap
+        assert p.last_device_status() != 0
+    with binding.Plan(0, wholek=2) as p:  # the context is still usable
         run_full(p, A, B, "bf16", exact=True)

@@ -458,7 +458,7 @@ def run_ours(args):
                 "frac_of_sustained_peak": (round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
                                            if roof["bound"] == "tensor" else None),
                 "traffic": recorded_traffic(shape.name),
-                "peak_source": (f"{peaks['source']} ({regime} cuBLAS bf16: timed region {total_s:.2f} s)"
+                "peak_source": (f"{peaks['source']} ({regime} cuBLAS bf16: timed region {total_s * 1e3:.1f} ms)"
                                 if roof["bound"] == "tensor" else f"{peaks['source']} (copy bandwidth)"),
                 "kernel": "bwgemm::gemm_kernel (persistent tcgen05)",
                 "algorithmic": (f"{shape.flops / 1e9:.1f} GFLOP per launch (2MNK)"

@@ -21,6 +21,10 @@ measures what that step of the design is worth here:
 - Split-K: slices in one cluster exchanging through distributed shared
   memory against slices reducing through L2.
 - Operand order for small M (C^T = B A^T).
+- The whole-K kernels: 64 weight rows per CTA for at most 64 rows of A
+  against split-K on 128-row tiles ("Writing a Blackwell GEMM by hand", "Two
+  workloads, not one"), and all rows of A on one CTA pair against the main
+  kernel for 129 to 256 rows.
 
 Steps fixed at compile time (128B swizzle, the ring depth, the TMEM
 double buffer) have no switch in the GEMM.  Two microbenchmarks cover the
@@ -67,16 +71,25 @@ ABLATIONS = [
     ("A multicast", {"multicast": 2}, "two pairs share each A tile"),
     ("split-K through L2", {"cluster_split": 1}, "clustered split-K exchange off"),
     ("operands in order", {"swap_ab": 1}, "C^T = B A^T off"),
+    ("whole-K kernel off", {"skinny": 1}, "split-K on 128-row tiles instead of 64 weight rows per CTA, whole K"),
+    ("whole-K pair kernel", {"wholek": 2}, "all rows of A on one CTA pair, narrow weight blocks, whole K"),
+    ("whole-K pair kernel off", {"wholek": 1}, "the main kernel instead of the whole-K pair kernel"),
 ]
 
-DEFAULT_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out", "tail_m64"]
+DEFAULT_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out", "decode_qkv", "tail_m64"]
 
 SHAPE_LABELS = {"square4096": "4096^3", "prefill_attn_out": "prefill 8192^3",
-                "decode_attn_out": "decode M=256 N=K=8192", "tail_m64": "tail M=64 N=K=8192"}
+                "decode_attn_out": "decode M=256 N=K=8192", "decode_qkv": "decode M=256 N=10240 K=8192",
+                "tail_m64": "tail M=64 N=K=8192"}
 
 
 def describe(cfg: dict) -> str:
     """Short description of a launch configuration (the default rows' label)."""
+    if cfg.get("skinny"):
+        form = "CTA pairs (M = 128)" if cfg.get("variant") == 2 else "1 CTA (M = 64)"
+        return f"whole-K, 64 weight rows per CTA, {form}, N = {cfg.get('tile_n')}"
+    if cfg.get("wholek"):
+        return f"whole-K pairs, all rows of A, {cfg.get('tile_n')} weight rows per pair"
     parts = ["swapped" if cfg.get("swap_ab") == 1 else None,
              "pairs" if cfg.get("variant") == 2 else "1 CTA",
              str(cfg.get("tile_n")),
@@ -109,7 +122,7 @@ def markdown_table(rows) -> str:
 PAGE_LOAD_PATH_TBS = {0: 18.5, 1: 3.85}
 LOAD_PATH_STAGES = 6
 LOAD_PATH_KBLOCKS = 4096
-EPILOGUE_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out"]
+EPILOGUE_SHAPES = ["square4096", "prefill_attn_out", "decode_attn_out", "decode_qkv", "tail_m64"]
 
 
 def load_path_table(rows) -> str:
@@ -309,7 +322,7 @@ def main(argv=None) -> int:
                         "roofline_frac": round(tflops / attainable, 4), "peak_source": peak_src,
                         "config": {k: cfg[k] for k in ("variant", "tile_n", "split_k", "schedule", "grid",
                                                        "copy_kblocks", "multicast", "cluster_split",
-                                                       "swap_ab", "raster_group")}})
+                                                       "swap_ab", "raster_group", "skinny", "wholek")}})
             if base_t is None:
                 base_t, base_cfg = t, cfg
             else:

@@ -106,6 +106,10 @@ def markdown(rows) -> str:
            "|---|---|---:|---|---:|---:|:---:|"]
     for r in rows:
         def d(c):
+            if c.get("skinny"):
+                return f"whole-K, 64 weight rows per CTA ({c['variant']}sm), N {c['tile_n']}"
+            if c.get("wholek"):
+                return f"whole-K pairs, {c['tile_n']} weight rows per pair"
             mc = "x2 multicast" if c.get("multicast") == 2 else ""
             sk = f"split {c['split_k']}" + (" in clusters" if c.get("cluster_split") else "") \
                 if c.get("split_k", 1) > 1 else {1: "tiles", 2: "stream-K", 3: "CLC"}.get(c.get("schedule"), "?")

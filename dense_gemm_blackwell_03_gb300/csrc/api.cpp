@@ -223,7 +223,7 @@ struct bwgemm_plan_s {
     // bwgemm_run_host's pipeline over row blocks: copy-in, GEMM and copy-out
     // streams and their events (created on first use)
     cudaStream_t side[3] = {nullptr, nullptr, nullptr};
-    cudaEvent_t events[2 * kHostChunksMax + 2] = {};
+    cudaEvent_t events[kHostEvents] = {};
     bool side_ready = false;
     // optional timeline (opts.trace): kTraceSlots stamps per CTA of the last launch
     uint64_t* d_trace = nullptr;
@@ -646,11 +646,17 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
     const int64_t rows = host_block_rows(M, N, K);
     const int chunks = rows > 0 ? int((M + rows - 1) / rows) : 1;
     if (chunks > 1) {
-        // Pipeline over row blocks of A and C: B goes over first, then row
-        // block i of A on the copy-in stream, its GEMM on the compute stream,
-        // and its rows of C back on the copy-out stream, so that the GEMMs and
-        // the copies of C overlap the copies of A (the link to host memory,
-        // not the GPU, bounds a call of this size).
+        // Pipeline over blocks of C: row block i of A and column block j of B
+        // (rows of B) come over on the copy-in stream in the order B0, A0, B1,
+        // ..., A1, A2, ...; GEMM (i, j) runs on the compute stream once both
+        // have landed, and row block i of C goes back on the copy-out stream
+        // after its last GEMM, so that the GEMMs and the copies of C overlap
+        // the copies still coming in (the link to host memory, not the GPU,
+        // bounds a call of this size).  The GEMMs run one after another on one
+        // stream: they share the plan's workspace.
+        const int64_t cols = host_block_cols(M, N, K);
+        const int cblocks = cols > 0 ? int((N + cols - 1) / cols) : 1;
+        const int64_t cw = cols > 0 ? cols : N;
         if (!plan->side_ready) {
             for (cudaStream_t& x : plan->side)
                 if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess)
@@ -661,30 +667,63 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
             plan->side_ready = true;
         }
         cudaStream_t s_in = plan->side[0], s_mm = plan->side[1], s_out = plan->side[2];
-        cudaEvent_t ev_start = plan->events[2 * kHostChunksMax];
-        cudaEvent_t ev_end = plan->events[2 * kHostChunksMax + 1];
-        if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(s_mm, ev_start, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess ||
-            copy_rows(plan->h2d[1], dlda, B_host, ldb, K, N, cudaMemcpyHostToDevice, s_in) != cudaSuccess)
-            return BWGEMM_ERR_CUDA;
+        cudaEvent_t* ev_a = plan->events;                              // [kHostChunksMax]
+        cudaEvent_t* ev_b = ev_a + kHostChunksMax;                     // [kHostColBlocksMax]
+        cudaEvent_t* ev_mm = ev_b + kHostColBlocksMax;                 // [kHostChunksMax][kHostColBlocksMax]
+        cudaEvent_t ev_start = ev_mm[kHostChunksMax * kHostColBlocksMax];
+        cudaEvent_t ev_end = ev_mm[kHostChunksMax * kHostColBlocksMax + 1];
         uint8_t* dA = static_cast<uint8_t*>(plan->h2d[0]);
+        uint8_t* dB = static_cast<uint8_t*>(plan->h2d[1]);
         uint8_t* dC = static_cast<uint8_t*>(plan->h2d[2]);
-        for (int i = 0; i < chunks; ++i) {
+        auto copy_a = [&](int i) {
             const int64_t r0 = i * rows, r = std::min<int64_t>(rows, M - r0);
-            if (r <= 0)
-                break;
-            cudaEvent_t ev_in = plan->events[2 * i], ev_mm = plan->events[2 * i + 1];
             const uint8_t* hA = static_cast<const uint8_t*>(A_host) + size_t(r0) * size_t(lda) * 2;
-            uint8_t* hC = static_cast<uint8_t*>(C_host) + size_t(r0) * size_t(ldc) * 2;
             if (copy_rows(dA + size_t(r0) * dlda * 2, dlda, hA, lda, K, r, cudaMemcpyHostToDevice, s_in) !=
                     cudaSuccess ||
-                cudaEventRecord(ev_in, s_in) != cudaSuccess || cudaStreamWaitEvent(s_mm, ev_in, 0) != cudaSuccess)
+                cudaEventRecord(ev_a[i], s_in) != cudaSuccess)
+                return false;
+            return true;
+        };
+        auto copy_b = [&](int j) {
+            const int64_t c0 = j * cw, c = std::min<int64_t>(cw, N - c0);
+            const uint8_t* hB = static_cast<const uint8_t*>(B_host) + size_t(c0) * size_t(ldb) * 2;
+            if (copy_rows(dB + size_t(c0) * dlda * 2, dlda, hB, ldb, K, c, cudaMemcpyHostToDevice, s_in) !=
+                    cudaSuccess ||
+                cudaEventRecord(ev_b[j], s_in) != cudaSuccess)
+                return false;
+            return true;
+        };
+        if (cudaEventRecord(ev_start, s) != cudaSuccess || cudaStreamWaitEvent(s_in, ev_start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_mm, ev_start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, ev_start, 0) != cudaSuccess)
+            return BWGEMM_ERR_CUDA;
+        // copy-in order: B0, A0, the other B blocks, then A1, A2, ...
+        if (!copy_b(0) || !copy_a(0))
+            return BWGEMM_ERR_CUDA;
+        for (int j = 1; j < cblocks; ++j)
+            if (!copy_b(j))
                 return BWGEMM_ERR_CUDA;
-            if ((st = enqueue(plan, opts, dA + size_t(r0) * dlda * 2, plan->h2d[1], dC + size_t(r0) * dldc * 2, r,
-                              N, K, dlda, dlda, dldc, dtype, s_mm)) != BWGEMM_OK)
-                return st;
-            if (cudaEventRecord(ev_mm, s_mm) != cudaSuccess || cudaStreamWaitEvent(s_out, ev_mm, 0) != cudaSuccess ||
+        for (int i = 1; i < chunks; ++i)
+            if (!copy_a(i))
+                return BWGEMM_ERR_CUDA;
+        for (int i = 0; i < chunks; ++i) {
+            const int64_t r0 = i * rows, r = std::min<int64_t>(rows, M - r0);
+            if (cudaStreamWaitEvent(s_mm, ev_a[i], 0) != cudaSuccess)
+                return BWGEMM_ERR_CUDA;
+            for (int j = 0; j < cblocks; ++j) {
+                const int64_t c0 = j * cw, c = std::min<int64_t>(cw, N - c0);
+                if (cudaStreamWaitEvent(s_mm, ev_b[j], 0) != cudaSuccess)
+                    return BWGEMM_ERR_CUDA;
+                if ((st = enqueue(plan, opts, dA + size_t(r0) * dlda * 2, dB + size_t(c0) * dlda * 2,
+                                  dC + (size_t(r0) * dldc + size_t(c0)) * 2, r, c, K, dlda, dlda, dldc, dtype,
+                                  s_mm)) != BWGEMM_OK)
+                    return st;
+            }
+            // the row block of C goes back whole (whole rows: one linear copy
+            // when the host rows are packed)
+            cudaEvent_t done = ev_mm[i * kHostColBlocksMax];
+            uint8_t* hC = static_cast<uint8_t*>(C_host) + size_t(r0) * size_t(ldc) * 2;
+            if (cudaEventRecord(done, s_mm) != cudaSuccess || cudaStreamWaitEvent(s_out, done, 0) != cudaSuccess ||
                 copy_rows(hC, ldc, dC + size_t(r0) * dldc * 2, dldc, N, r, cudaMemcpyDeviceToHost, s_out) !=
                     cudaSuccess)
                 return BWGEMM_ERR_CUDA;

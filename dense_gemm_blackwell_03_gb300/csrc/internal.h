@@ -71,6 +71,15 @@ cudaError_t variant_max_active(int idx, int* out);
 // are split (below that the copies are too short to hide a GEMM behind).
 constexpr int kHostChunksMax = 8;
 int64_t host_block_rows(int64_t M, int64_t N, int64_t K);
+// ... and its columns of C (rows of B) per block when the rows are split:
+// N in kHostColBlocksMax blocks of whole 256-column tiles once N >= 2048 and
+// a block of C still holds 64 tiles of 256 x 256 (0: one block), so that the
+// first GEMM waits for half of B instead of all of it and the copies of C
+// start that much earlier.
+constexpr int kHostColBlocksMax = 2;
+int64_t host_block_cols(int64_t M, int64_t N, int64_t K);
+// events of the pipeline: A blocks in, B blocks in, GEMMs done, start, end
+constexpr int kHostEvents = kHostChunksMax + kHostColBlocksMax + kHostChunksMax * kHostColBlocksMax + 2;
 
 // BWGEMM_OK when every operand a call reads or writes (A and B only when
 // K > 0) is device or managed memory of `device`; BWGEMM_ERR_INVALID_ARG

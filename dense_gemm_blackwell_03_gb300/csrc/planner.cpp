@@ -492,6 +492,19 @@ int64_t host_block_rows(int64_t M, int64_t N, int64_t K)
     return rows < M ? rows : 0;
 }
 
+int64_t host_block_cols(int64_t M, int64_t N, int64_t K)
+{
+    const int64_t rows = host_block_rows(M, N, K);
+    if (rows == 0 || N < 2048)
+        return 0;
+    const int64_t cols = ceil_div(ceil_div(N, int64_t(kHostColBlocksMax)), 256) * 256;
+    // only blocks that still fill the GPU (64 tiles of 256 x 256): smaller
+    // GEMMs run too far below the peak for the earlier start to pay
+    if (cols >= N || rows * cols < int64_t(64) * 256 * 256)
+        return 0;
+    return cols;
+}
+
 GemmParams make_params(const Selection& sel, int64_t M, int64_t N, int64_t K, bwgemm_dtype_t dtype)
 {
     GemmParams p;

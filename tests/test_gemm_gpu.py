@@ -550,12 +550,14 @@ def test_host_buffers_round_trip(plan):
     compare(bits_of(C), ref, "bf16", 264, exact=True)
 
 
-@pytest.mark.parametrize("M,lda_pad,ldc_pad", [(2000, 0, 0), (1536, 8, 16), (1100, 24, 0)])
-def test_host_buffers_pipelined(M, lda_pad, ldc_pad):
-    # calls moving >= 16 MiB run as a pipeline over row blocks (A in, GEMM, C
-    # out on three streams); ragged last block, host strides wider than the
-    # rows, run twice on one plan
-    K, N = 2048, 2048
+@pytest.mark.parametrize("M,N,K,lda_pad,ldc_pad", [(2000, 2048, 2048, 0, 0), (1536, 2048, 2048, 8, 16),
+                                                   (1100, 2048, 2048, 24, 0), (8192, 7800, 512, 0, 8),
+                                                   (1024, 1024, 2048, 0, 0)])
+def test_host_buffers_pipelined(M, N, K, lda_pad, ldc_pad):
+    # calls moving >= 16 MiB run as a pipeline over blocks of C (row blocks of
+    # A and, once a block of C holds 64 tiles of 256 x 256, two column blocks
+    # of B: A and B in, GEMM, C out on three streams); ragged last row and
+    # column blocks, host strides wider than the rows, run twice on one plan
     Abuf = make_matrix(M, K + lda_pad, "int2", seed=940 + M).pin_memory()
     A = Abuf[:, :K]
     B = make_matrix(N, K, "int2", seed=941).pin_memory()

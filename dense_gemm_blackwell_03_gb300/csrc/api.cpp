@@ -643,8 +643,8 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
                                  size_t(rows), kind, cs);
     };
     const bwgemm_plan_options_t& opts = options_for(plan, M, N, K, dtype);
-    const int64_t rows = host_block_rows(M, N, K);
-    const int chunks = rows > 0 ? int((M + rows - 1) / rows) : 1;
+    int64_t starts[kHostChunksMax + 1];
+    const int chunks = host_row_blocks(M, N, K, starts);
     if (chunks > 1) {
         // Pipeline over blocks of C: row block i of A and column block j of B
         // (rows of B) come over on the copy-in stream in the order B0, A0, B1,
@@ -676,7 +676,7 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
         uint8_t* dB = static_cast<uint8_t*>(plan->h2d[1]);
         uint8_t* dC = static_cast<uint8_t*>(plan->h2d[2]);
         auto copy_a = [&](int i) {
-            const int64_t r0 = i * rows, r = std::min<int64_t>(rows, M - r0);
+            const int64_t r0 = starts[i], r = starts[i + 1] - starts[i];
             const uint8_t* hA = static_cast<const uint8_t*>(A_host) + size_t(r0) * size_t(lda) * 2;
             if (copy_rows(dA + size_t(r0) * dlda * 2, dlda, hA, lda, K, r, cudaMemcpyHostToDevice, s_in) !=
                     cudaSuccess ||
@@ -707,7 +707,7 @@ bwgemm_status_t bwgemm_run_host(bwgemm_plan_t plan, const void* A_host, const vo
             if (!copy_a(i))
                 return BWGEMM_ERR_CUDA;
         for (int i = 0; i < chunks; ++i) {
-            const int64_t r0 = i * rows, r = std::min<int64_t>(rows, M - r0);
+            const int64_t r0 = starts[i], r = starts[i + 1] - starts[i];
             if (cudaStreamWaitEvent(s_mm, ev_a[i], 0) != cudaSuccess)
                 return BWGEMM_ERR_CUDA;
             for (int j = 0; j < cblocks; ++j) {

@@ -65,12 +65,15 @@ cudaError_t launch_variant(int idx, const CUtensorMap& a, const CUtensorMap& b, 
 // variant `idx` on the current device.
 cudaError_t variant_max_active(int idx, int* out);
 
-// bwgemm_run_host: rows of A and C per block of its copy/compute pipeline
-// (0: one block, no pipeline).  Blocks are whole 256-row tiles, at least 512
-// rows, at most kHostChunksMax of them, and only calls that move >= 16 MiB
-// are split (below that the copies are too short to hide a GEMM behind).
-constexpr int kHostChunksMax = 8;
-int64_t host_block_rows(int64_t M, int64_t N, int64_t K);
+// bwgemm_run_host: the row blocks of A and C of its copy/compute pipeline.
+// Calls that move >= 16 MiB with M >= 1024 are split into blocks of whole
+// 256-row tiles, 1024 rows from M = 2048 (512 below), at most
+// kHostChunksMax of them, the last one halved so that the GEMM and the copy of
+// C that nothing overlaps at the end are short.  host_row_blocks writes the
+// first row of each block and M after the last into starts[] (room for
+// kHostChunksMax + 1) and returns the number of blocks (1: no pipeline).
+constexpr int kHostChunksMax = 12;
+int host_row_blocks(int64_t M, int64_t N, int64_t K, int64_t* starts);
 // ... and its columns of C (rows of B) per block when the rows are split:
 // N in kHostColBlocksMax blocks of whole 256-column tiles once N >= 2048 and
 // a block of C still holds 64 tiles of 256 x 256 (0: one block), so that the

@@ -482,19 +482,49 @@ bwgemm_status_t select_config(int num_sms, int max_pairs, int max_quads, int64_t
     return BWGEMM_OK;
 }
 
-int64_t host_block_rows(int64_t M, int64_t N, int64_t K)
+namespace {
+
+// rows of a full block of bwgemm_run_host's pipeline (0: no pipeline)
+int64_t host_base_rows(int64_t M, int64_t N, int64_t K)
 {
     const int64_t bytes = 2 * (M * K + N * K + M * N);
     if (K <= 0 || N <= 0 || M < 1024 || bytes < (int64_t(16) << 20))
         return 0;
-    const int64_t blocks = std::min<int64_t>(kHostChunksMax, M / 512);
-    const int64_t rows = ceil_div(ceil_div(M, blocks), 256) * 256;
+    int64_t rows = M >= 2048 ? 1024 : 512;
+    // at most kHostChunksMax - 1 full blocks (the last one is halved)
+    rows = std::max<int64_t>(rows, ceil_div(ceil_div(M, int64_t(kHostChunksMax - 1)), 256) * 256);
     return rows < M ? rows : 0;
+}
+
+}  // namespace
+
+int host_row_blocks(int64_t M, int64_t N, int64_t K, int64_t* starts)
+{
+    const int64_t rows = host_base_rows(M, N, K);
+    starts[0] = 0;
+    if (rows == 0) {
+        starts[1] = M;
+        return 1;
+    }
+    int n = 0;
+    while (starts[n] + rows < M) {
+        starts[n + 1] = starts[n] + rows;
+        ++n;
+    }
+    // the last block: M - starts[n] rows, halved (whole 256-row tiles) when it
+    // holds at least two tiles
+    const int64_t last = M - starts[n];
+    if (last >= 512) {
+        starts[n + 1] = starts[n] + ceil_div(last / 2, int64_t(256)) * 256;
+        ++n;
+    }
+    starts[n + 1] = M;
+    return n + 1;
 }
 
 int64_t host_block_cols(int64_t M, int64_t N, int64_t K)
 {
-    const int64_t rows = host_block_rows(M, N, K);
+    const int64_t rows = host_base_rows(M, N, K);
     if (rows == 0 || N < 2048)
         return 0;
     const int64_t cols = ceil_div(ceil_div(N, int64_t(kHostColBlocksMax)), 256) * 256;

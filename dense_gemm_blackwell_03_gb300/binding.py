@@ -213,13 +213,26 @@ def make_options(**kw) -> PlanOptions:
     return o
 
 
+_torch_mod = None
+_dtype_codes: dict = {}
+
+
+def _torch():
+    """The torch module, imported once (the per-call path looks it up here)."""
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+        _dtype_codes.update({torch.bfloat16: BF16, torch.float16: FP16})
+    return _torch_mod
+
+
 def _dtype_code(t) -> int:
-    import torch
-    if t.dtype == torch.bfloat16:
-        return BF16
-    if t.dtype == torch.float16:
-        return FP16
-    raise TypeError(f"bwgemm takes bfloat16 or float16 tensors, got {t.dtype}")
+    _torch()
+    code = _dtype_codes.get(t.dtype)
+    if code is None:
+        raise TypeError(f"bwgemm takes bfloat16 or float16 tensors, got {t.dtype}")
+    return code
 
 
 def _ld(t) -> int:
@@ -328,23 +341,29 @@ class Plan:
 
     def gemm(self, A, B, out=None, stream=None):
         """``out = A @ B.T`` for CUDA bf16/fp16 tensors A (M x K) and B (N x K)."""
-        import torch
+        torch = _torch()
         dt = _dtype_code(A)
         if B.dtype != A.dtype:
             raise TypeError("A and B must have the same dtype")
-        if not (A.is_cuda and B.is_cuda):
-            raise ValueError("A and B must be CUDA tensors (bwgemm has no host path)")
+        dev = self.device
+        # get_device(): the CUDA device index, -1 for host tensors
+        if A.get_device() != dev or B.get_device() != dev:
+            if not (A.is_cuda and B.is_cuda):
+                raise ValueError("A and B must be CUDA tensors (bwgemm has no host path)")
+            self._check_device(A, B)
         M, K = A.shape
         N, Kb = B.shape
         if Kb != K:
             raise ValueError(f"K mismatch: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
         if out is None:
             out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-        elif out.dtype != A.dtype or tuple(out.shape) != (M, N) or not out.is_cuda:
-            raise ValueError("out must be an M x N CUDA tensor of the operands' dtype")
-        self._check_device(A, B, out)
+        elif out.dtype != A.dtype or out.shape != (M, N) or out.get_device() != dev:
+            if out.dtype != A.dtype or tuple(out.shape) != (M, N) or not out.is_cuda:
+                raise ValueError("out must be an M x N CUDA tensor of the operands' dtype")
+            self._check_device(A, B, out)
+        s = (torch.cuda.current_stream(dev) if stream is None else stream).cuda_stream
         rc = self.lib.bwgemm_run(self.handle, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                                 _ld(A), _ld(B), _ld(out), dt, self._stream_handle(stream))
+                                 _ld(A), _ld(B), _ld(out), dt, s)
         if rc != 0:
             raise BwgemmError(rc, "bwgemm_run")
         return out

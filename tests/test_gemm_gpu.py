@@ -883,3 +883,27 @@ def test_wholek_bounded_wait_reports_timeout():
         assert p.last_device_status() != 0
     with binding.Plan(0, wholek=2) as p:  # the context is still usable
         run_full(p, A, B, "bf16", exact=True)
+
+
+@pytest.mark.parametrize("M,opts", [(16, {}), (64, {}), (200, {"wholek": 2})])
+def test_whole_k_kernels_without_programmatic_dependent_launch(M, opts):
+    # plain stream order between launches (no griddepcontrol overlap)
+    A = make_matrix(M, 1000, "int2", seed=5600 + M, device="cuda")
+    B = make_matrix(2048, 1000, "int2", seed=5601, device="cuda")
+    with binding.Plan(0, pdl_off=1, **opts) as p:
+        for _ in range(3):
+            run_full(p, A, B, "bf16", exact=True)
+        c = p.last_config()
+        assert c["skinny"] == 1 if M <= 64 else c["wholek"] == 1
+
+
+@pytest.mark.parametrize("M", [16, 200])
+def test_tune_on_whole_k_shapes(M):
+    # the tuner's candidates on a decode-batch shape: whatever it keeps is exact
+    A = make_matrix(M, 1024, "int2", seed=5700 + M, device="cuda")
+    B = make_matrix(2048, 1024, "int2", seed=5701, device="cuda")
+    C = torch.zeros((M, 2048), dtype=torch.bfloat16, device="cuda")
+    with binding.Plan(0) as p:
+        p.tune(A, B, out=C, iters=3)
+        assert p.tuned_count() == 1
+        run_full(p, A, B, "bf16", exact=True)
